@@ -1,0 +1,315 @@
+"""Benchmark of the paged, quantised-KV attention path on one GB300.
+
+One step = the whole path over one batch: pa_run (attention over the paged
+int8 / FP8 cache, split-KV partials) + pa_merge (log-sum-exp merge), with the
+plan already uploaded and every input resident in HBM.  The default workload is
+decode-2 (bsz 64, q_len 1, 32 q heads / 8 kv heads, head dim 128, int8
+per-channel scales, prefix U[512, 4096], 4096-page shuffled pool, chunk 512);
+the metric is algorithmic KV-cache bytes (every visible (page, head) slab read
+once) per second.  --config 4 runs spec-verify-4 (same metric).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|4] [--impl reference]
+
+Prints one JSON line.  For N > 1 it runs under torch.distributed (one process
+per GPU); each rank runs an independent replica of the workload (the path has
+no cross-GPU exchange), time = max over ranks, value = all ranks' bytes / time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "KV-cache HBM GB/s (decode) & TFLOP/s (append/MLA), % of GB300 roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch.distributed as dist
+    backend = "nccl"
+    dist.init_process_group(backend=backend)
+    return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _workload(config: int):
+    import synth
+    case = synth.config(config)
+    return case
+
+
+def run_cuda(args) -> dict:
+    import torch
+    import paged_quantized_kv_gqa_gb300 as pa
+    from synth.device import to_device
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    case = _workload(args.config)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    d = to_device(case, dev)
+    plan = pa.pa_plan(pa.problem_of(case), case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, sms)
+    desc = plan.describe()
+    ws = torch.zeros(plan.workspace_size, dtype=torch.uint8, device=dev)
+    cargs = pa.make_args(q=d["q"], cache_k=d["cache_k"], cache_v=d["cache_v"],
+                         k_scale=d["k_scale"], v_scale=d["v_scale"], block_table=d["block_table"],
+                         out=d["out"], lse=d["lse"])
+    stream = torch.cuda.current_stream(dev)
+    pa.pa_plan_upload(plan, ws, stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    split = desc["max_chunks"] > 1
+
+    def step():
+        pa.pa_run(plan, cargs, ws, stream)
+        if split:
+            pa.pa_merge(plan, cargs, ws, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    st, det = pa.pa_check(plan, ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)              # evict the cache from L2 between steps
+            a, m, b = ev[i]
+            a.record(stream)
+            pa.pa_run(plan, cargs, ws, stream)
+            m.record(stream)
+            if split:
+                pa.pa_merge(plan, cargs, ws, stream)
+            b.record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(world)
+    step_ms = [a.elapsed_time(b) for a, _, b in ev]
+    run_ms = [a.elapsed_time(m) for a, m, _ in ev]
+    ms = statistics.mean(step_ms)
+    ms_max = _max_over_ranks(ms, world)
+    kv_bytes = desc["kv_bytes"]
+    value = kv_bytes * world / (ms_max * 1e-3) / 1e9
+    run_mean = statistics.mean(run_ms)
+    peak, peak_kind = _peaks()
+    achieved = kv_bytes / (run_mean * 1e-3) / 1e9
+    st, det = pa.pa_check(plan, ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+
+    # end to end through the public API with host buffers: q / lengths / table up,
+    # plan upload, run, merge, out + lse down, all inside the timed region
+    q_h = d["q"].cpu().pin_memory()
+    bt_h = d["block_table"].cpu().pin_memory()
+    out_h = torch.empty_like(d["out"], device="cpu").pin_memory()
+    lse_h = torch.empty_like(d["lse"], device="cpu").pin_memory()
+    plan_words = (desc["num_ctas"] + 1) + desc["num_items"] * 8 + desc["total_q"] + \
+        len(desc["merge_tokens"])
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + plan_words * 4
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
+    e2e_ms = []
+    for i in range(max(3, K)):
+        flush.fill_(i & 0xFF)
+        a, _, b = ev[i % K]
+        a.record(stream)
+        d["q"].copy_(q_h, non_blocking=True)
+        d["block_table"].copy_(bt_h, non_blocking=True)
+        pa.pa_plan_upload(plan, ws, stream)
+        step()
+        out_h.copy_(d["out"], non_blocking=True)
+        lse_h.copy_(d["lse"], non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = kv_bytes * world / (_max_over_ranks(statistics.mean(e2e_ms), world) * 1e-3) / 1e9
+
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16 (int8 KV dequantised exactly; fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": case.name, "desc": synth_desc(args.config),
+                   "kv_bytes_per_step": kv_bytes, "items": desc["num_items"],
+                   "ctas": desc["num_ctas"], "chunk": desc["chunk"],
+                   "l2": "flushed (512 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "pa_run attention kernel",
+                     "run_ms": round(run_mean, 5)},
+        "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": K * (2 if split else 1),
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+    return res if rank == 0 else None
+
+
+def synth_desc(n: int) -> str:
+    import synth
+    return synth.CONFIG_NAMES[n]
+
+
+def cpu_baseline(case, seconds: float) -> dict:
+    """The fp64 oracle as it stands, on a bounded sample of (sequence, kv head) units."""
+    from oracle import attention as oa
+    units = [(b, h) for b in range(case.bsz) for h in range(case.kv_heads)]
+    rng = np.random.default_rng(0)
+    rng.shuffle(units)
+    done_bytes = 0
+    per_unit = lambda b: int(np.ceil((case.seq_lens_kv[b] + case.seq_lens[b]) / case.block_size)) \
+        * case.block_size * (case.head_dim_qk + case.head_dim_v)
+    t0 = time.perf_counter()
+    n = 0
+    for b, h in units:
+        oa.unit_attention(case, b, h)
+        done_bytes += per_unit(b)
+        n += 1
+        if time.perf_counter() - t0 > seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(done_bytes / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} of {len(units)} (sequence, kv head) units of {case.name}, "
+                      f"{dt:.1f} s, numpy fp64 (single-threaded gather/einsum)"}
+
+
+def run_reference(args) -> dict:
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    case = _workload(args.config)
+    K, W = args.steps, args.warmup
+    per = max(1.0, args.cpu_seconds / max(1, K + W))
+    vals = []
+    for i in range(W + K):
+        cb = cpu_baseline(case, per)
+        if i >= W:
+            vals.append(cb["value"])
+    v = statistics.mean(vals)
+    cb["value"] = round(v, 6)
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s",
+            "n_gpus": 1, "steps": K, "warmup": W, "higher_is_better": True,
+            "ms_per_step": None, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": case.name, "desc": synth_desc(args.config)},
+            "cpu_baseline": cb,
+            "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2, choices=[2, 4])
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    res = run_reference(args) if args.impl == "reference" else run_cuda(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

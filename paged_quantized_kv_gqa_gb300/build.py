@@ -1,0 +1,83 @@
+"""Builds the CUDA library (libpa_gb300.so) in-tree with nvcc for sm_103a.
+
+Translation units compile in parallel, then link into one shared library next
+to this file.  The seeded input generator (synth/csrc) is built the same way
+into synth/libpa_synth.so.  Rebuilds only when a source is newer than the
+library.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+LIB = os.path.join(PKG, "libpa_gb300.so")
+SYNTH_SRC = os.path.join(ROOT, "synth", "csrc", "synth_gen.cu")
+SYNTH_LIB = os.path.join(ROOT, "synth", "libpa_synth.so")
+BUILD_DIR = os.path.join(ROOT, "_build")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
+         "-Xptxas", "-warn-spills"]
+
+
+def _nvcc() -> str:
+    cuda = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    p = os.path.join(cuda, "bin", "nvcc")
+    return p if os.path.exists(p) else (shutil.which("nvcc") or "nvcc")
+
+
+def _sources():
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+
+
+def _headers():
+    hs = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
+    return hs + [os.path.join(INCLUDE, "pa.h")]
+
+
+def _stale(target, deps) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def _run(cmd):
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("build failed: " + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+    return r.stdout + r.stderr
+
+
+def build(verbose: bool = False, force: bool = False) -> str:
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    nvcc = _nvcc()
+    srcs = _sources()
+    deps = srcs + _headers()
+    if force or _stale(LIB, deps):
+        objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
+        cmds = [[nvcc, *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", s, "-o", o]
+                for s, o in zip(srcs, objs)]
+        with cf.ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 4))) as ex:
+            logs = list(ex.map(_run, cmds))
+        if verbose:
+            for lg in logs:
+                print(lg)
+        tmp = LIB + ".tmp"
+        _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs])
+        os.replace(tmp, LIB)
+    if force or _stale(SYNTH_LIB, [SYNTH_SRC]):
+        tmp = SYNTH_LIB + ".tmp"
+        _run([nvcc, *ARCH, *FLAGS, "-shared", "-cudart", "shared", SYNTH_SRC, "-o", tmp])
+        os.replace(tmp, SYNTH_LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    print(build(verbose=True))

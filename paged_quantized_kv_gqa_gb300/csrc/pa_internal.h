@@ -1,0 +1,103 @@
+// pa_internal.h - structures shared by the host API and the kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "pa.h"
+
+namespace pa {
+
+constexpr int kItemWords = 8;        // b, kvh, token0, n_tok, causal_base, kv0, kv1, c|nch<<16
+constexpr int kDecodeRows = 64;      // packed (token, head) rows per decode tile
+constexpr int kAppendRows = 128;     // packed rows per append tile
+constexpr int kStatusBytes = 256;    // status block at the start of the workspace
+constexpr int64_t kDefaultWaitNs = 2000000000LL;
+
+// Status block layout (int32 words): [0] status code, [1] detail, [2] cta, [3] spare.
+
+struct Plan {
+  pa_problem prob{};
+  int32_t family = 0;
+  int32_t chunk = 0;
+  int32_t tokens_per_tile = 0;
+  int32_t num_ctas = 0;
+  int32_t total_q = 0;
+  int32_t max_chunks = 1;
+  int32_t num_sms = 0;
+  int32_t decode_rows = 0;    // padded row count (decode family)
+  std::vector<int32_t> items;        // [n][8] CTA-major
+  std::vector<int32_t> work_indptr;  // [num_ctas+1]
+  std::vector<int32_t> nch_token;    // [T]
+  std::vector<int32_t> merge_tokens; // [n_merge]
+  // device blob = work_indptr | items | nch_token | merge_tokens (int32), at kStatusBytes
+  std::vector<int32_t> blob;
+  size_t off_indptr = 0, off_items = 0, off_nch = 0, off_merge = 0;  // int32 offsets in blob
+  size_t plan_bytes = 0;
+  size_t part_o_off = 0, part_m_off = 0, part_d_off = 0, ws_bytes = 0;  // byte offsets
+  int64_t kv_bytes = 0;
+  double flops = 0.0;
+  int32_t num_items() const { return (int32_t)(items.size() / kItemWords); }
+};
+
+// Device pointers derived from a workspace.
+struct WsView {
+  int32_t* status;
+  const int32_t* work_indptr;
+  const int32_t* items;
+  const int32_t* nch_token;
+  const int32_t* merge_tokens;
+  __nv_bfloat16* part_o;
+  float* part_m;
+  float* part_d;
+};
+
+struct FaultCfg {
+  int64_t wait_limit_ns;
+  int32_t skip_first_load;
+};
+
+// Kernel parameter block for the attention kernels (passed by value).
+struct AttnParams {
+  const int32_t* items;
+  const int32_t* work_indptr;
+  const int32_t* block_table;
+  const __nv_bfloat16* q;
+  const void* k_scale;
+  const void* v_scale;
+  __nv_bfloat16* out;
+  float* lse;
+  __nv_bfloat16* part_o;
+  float* part_m;
+  float* part_d;
+  int32_t* status;
+  int64_t q_stride;
+  int64_t wait_limit_ns;
+  int32_t max_blocks;
+  int32_t num_pages;
+  int32_t q_heads;
+  int32_t kv_heads;
+  int32_t group;
+  int32_t scale_kind;
+  int32_t max_chunks;
+  int32_t skip_first_load;
+  float sm_scale_log2;   // sm_scale * log2(e)
+};
+
+void set_error(const std::string& msg);
+
+// launchers (return a cudaError_t from the launch)
+cudaError_t launch_decode(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, cudaStream_t stream);
+cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
+                         cudaStream_t stream);
+cudaError_t launch_gather(const pa_problem& prob, const pa_args& a, int32_t b, int32_t kvh,
+                          int32_t pos0, int32_t n, void* dk, void* dv, cudaStream_t stream);
+
+}  // namespace pa

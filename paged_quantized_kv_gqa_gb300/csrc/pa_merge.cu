@@ -1,0 +1,141 @@
+// pa_merge.cu - split-KV partial-state merge and the raw-gather test hook.
+//
+// Merge (FastDeploy append_attention_c8_impl.cuh, merge_multi_chunks_*_kernel
+// launched after the split kernel; FlashInfer persistent.cuh,
+// BlockBatchReductionPersistent; XQA mla_sm120.cu, mergePartialOutputs):
+// for a query row with chunk states (o_c, m_c, d_c), o_c normalised,
+//   M = max_c m_c,  w_c = d_c * exp(m_c - M),
+//   out = sum_c w_c o_c / sum_c w_c,  lse = M + log(sum_c w_c).
+// One warp per (token, query head); the partial states of a token sit at
+// slot (token * max_chunks + c) * q_heads + head.  HBM-bound, CUDA cores.
+#include <cfloat>
+
+#include "pa_internal.h"
+#include "pa_index.cuh"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+template <int DV>
+__global__ void __launch_bounds__(256) merge_kernel(const int32_t* __restrict__ merge_tokens,
+                                                    const int32_t* __restrict__ nch_token,
+                                                    int n_merge, int q_heads, int max_chunks,
+                                                    const __nv_bfloat16* __restrict__ part_o,
+                                                    const float* __restrict__ part_m,
+                                                    const float* __restrict__ part_d,
+                                                    __nv_bfloat16* __restrict__ out,
+                                                    float* __restrict__ lse) {
+  constexpr int kPer = DV / 32;  // elements per lane
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (wid >= n_merge * q_heads) return;
+  const int token = merge_tokens[wid / q_heads];
+  const int head = wid % q_heads;
+  const int nch = nch_token[token];
+  const int64_t slot0 = (int64_t)token * max_chunks * q_heads + head;
+
+  float M = -INFINITY;
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, part_m[slot0 + (int64_t)c * q_heads]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  float W = 0.f;
+  if (M != -INFINITY) {
+    for (int c = 0; c < nch; ++c) {
+      const int64_t slot = slot0 + (int64_t)c * q_heads;
+      const float mc = part_m[slot];
+      if (mc == -INFINITY) continue;
+      const float w = part_d[slot] * __expf(mc - M);
+      W += w;
+      const __nv_bfloat16* src = part_o + slot * DV + lane * kPer;
+#pragma unroll
+      for (int k = 0; k < kPer; k += 4) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src + k);
+        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+        acc[k + 0] += w * __low2float(a);
+        acc[k + 1] += w * __high2float(a);
+        acc[k + 2] += w * __low2float(b);
+        acc[k + 3] += w * __high2float(b);
+      }
+    }
+  }
+  const float inv = W > 0.f ? 1.0f / W : 0.f;
+  __nv_bfloat16* dst = out + ((int64_t)token * q_heads + head) * DV + lane * kPer;
+#pragma unroll
+  for (int k = 0; k < kPer; k += 4) {
+    __nv_bfloat162 a = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
+    __nv_bfloat162 b = __floats2bfloat162_rn(acc[k + 2] * inv, acc[k + 3] * inv);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t*>(&a);
+    raw.y = *reinterpret_cast<uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(dst + k) = raw;
+  }
+  if (lse != nullptr && lane == 0)
+    lse[(int64_t)token * q_heads + head] = W > 0.f ? M + __logf(W) : -INFINITY;
+}
+
+cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
+                         cudaStream_t stream) {
+  const int n_merge = (int)plan.merge_tokens.size();
+  if (n_merge == 0) return cudaSuccess;
+  const int warps = n_merge * plan.prob.q_heads;
+  const int blocks = (warps + 7) / 8;
+  if (plan.prob.head_dim_v == 128) {
+    merge_kernel<128><<<blocks, 256, 0, stream>>>(ws.merge_tokens, ws.nch_token, n_merge,
+                                                 plan.prob.q_heads, plan.max_chunks, ws.part_o,
+                                                 ws.part_m, ws.part_d, out, lse);
+  } else if (plan.prob.head_dim_v == 512) {
+    merge_kernel<512><<<blocks, 256, 0, stream>>>(ws.merge_tokens, ws.nch_token, n_merge,
+                                                 plan.prob.q_heads, plan.max_chunks, ws.part_o,
+                                                 ws.part_m, ws.part_d, out, lse);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ gather
+__global__ void gather_kernel(const uint8_t* __restrict__ cache_k, const uint8_t* __restrict__ cache_v,
+                              const int32_t* __restrict__ block_table, int max_blocks, int num_pages,
+                              int kv_heads, int page_size, int dqk, int dv, int mla, int b, int kvh,
+                              int pos0, int n, uint8_t* __restrict__ dk, uint8_t* __restrict__ dv_out) {
+  const int k = blockIdx.x;
+  if (k >= n) return;
+  const int pos = pos0 + k;
+  const int page = page_of(block_table, max_blocks, b, pos, page_size);
+  const int off = pos % page_size;
+  const bool ok = page >= 0 && page < num_pages;
+  for (int e = threadIdx.x; e < dqk; e += blockDim.x) {
+    uint8_t v = 0;
+    if (ok) {
+      v = mla ? cache_k[((int64_t)page * page_size + off) * dqk + e]
+              : cache_k[(((int64_t)page * kv_heads + kvh) * page_size + off) * dqk + e];
+    }
+    dk[(int64_t)k * dqk + e] = v;
+  }
+  for (int e = threadIdx.x; e < dv; e += blockDim.x) {
+    uint8_t v = 0;
+    if (ok) {
+      v = mla ? cache_k[((int64_t)page * page_size + off) * dqk + e]
+              : cache_v[(((int64_t)page * kv_heads + kvh) * dv + e) * page_size + off];
+    }
+    dv_out[(int64_t)k * dv + e] = v;
+  }
+}
+
+cudaError_t launch_gather(const pa_problem& prob, const pa_args& a, int32_t b, int32_t kvh,
+                          int32_t pos0, int32_t n, void* dk, void* dv, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  gather_kernel<<<n, 128, 0, stream>>>(
+      static_cast<const uint8_t*>(a.cache_k), static_cast<const uint8_t*>(a.cache_v),
+      a.block_table, prob.max_blocks_per_seq, prob.num_pages, prob.kv_heads, prob.block_size,
+      prob.head_dim_qk, prob.head_dim_v, prob.layout == PA_LAYOUT_MLA ? 1 : 0, b, kvh, pos0, n,
+      static_cast<uint8_t*>(dk), static_cast<uint8_t*>(dv));
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -83,6 +83,7 @@ class Case:
     int8_range: tuple = (-127, 127)
     _cache_k: Optional[np.ndarray] = None
     _cache_v: Optional[np.ndarray] = None
+    _page_memo: Optional[dict] = None
 
     # ----- derived sizes -------------------------------------------------
     @property
@@ -155,14 +156,23 @@ class Case:
 
     def page_k(self, page: int) -> np.ndarray:
         """One physical page of K (all kv heads), regenerated without the rest."""
-        shape = self.k_shape[1:]
-        n = int(np.prod(shape))
-        return self.kv_bytes("k", page * n, n).reshape(shape)
+        return self._page("k", page)
 
     def page_v(self, page: int) -> np.ndarray:
-        shape = self.v_shape[1:]
-        n = int(np.prod(shape))
-        return self.kv_bytes("v", page * n, n).reshape(shape)
+        return self._page("v", page)
+
+    def _page(self, which: str, page: int) -> np.ndarray:
+        if self._page_memo is None:
+            self._page_memo = {}
+        key = (which, int(page))
+        got = self._page_memo.get(key)
+        if got is None:
+            shape = (self.k_shape if which == "k" else self.v_shape)[1:]
+            n = int(np.prod(shape))
+            got = self.kv_bytes(which, int(page) * n, n).reshape(shape)
+            if len(self._page_memo) < 200_000:
+                self._page_memo[key] = got
+        return got
 
     def kv_bytes_total(self) -> int:
         """Cache bytes the attention must read once: every visible (page, head) slab."""

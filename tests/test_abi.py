@@ -1,0 +1,146 @@
+"""CPU checks of the C ABI: the library loads, exports every declared entry
+point, validates arguments before any launch, and its planner reproduces the
+oracle planner bit for bit."""
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import planner as op
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pa():
+    import paged_quantized_kv_gqa_gb300 as m
+    return m
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(pa):
+    names = declared_functions()
+    assert "pa_plan" in names and "pa_run" in names and "pa_merge" in names
+    for n in names:
+        assert hasattr(pa.lib, n), n
+
+
+def _plan(pa, case, sms=152):
+    return pa.pa_plan(pa.problem_of(case), case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, sms)
+
+
+CASES = [
+    dict(seq_lens=[3, 1], seq_lens_kv=[70, 0], q_heads=8, kv_heads=2, chunk_size=64),
+    dict(seq_lens=[1] * 9, seq_lens_kv=list(range(0, 900, 100)), q_heads=32, kv_heads=8,
+         chunk_size=128, causal=False),
+    dict(seq_lens=[40, 0, 17], seq_lens_kv=[5, 9, 300], q_heads=8, kv_heads=2, chunk_size=0),
+    dict(seq_lens=[200, 3], seq_lens_kv=[1000, 4000], q_heads=32, kv_heads=8, chunk_size=256),
+    dict(seq_lens=[6] * 5, seq_lens_kv=[8000, 9000, 100, 64, 63], q_heads=64, kv_heads=8,
+         chunk_size=1024),
+    dict(seq_lens=[1, 2, 2], seq_lens_kv=[4000, 9000, 17], q_heads=128, kv_heads=1,
+         head_dim_qk=576, head_dim_v=512, kv_dtype="fp8_e4m3", scale_kind="global",
+         layout="mla", chunk_size=-1),
+    dict(seq_lens=[5, 7], seq_lens_kv=[3000, 10], q_heads=16, kv_heads=4, chunk_size=-1),
+]
+
+
+@pytest.mark.parametrize("kw", CASES)
+@pytest.mark.parametrize("sms", [1, 7, 152])
+def test_planner_matches_oracle(pa, kw, sms):
+    case = synth.make_case(name="p", seed=5, **kw)
+    got = _plan(pa, case, sms).describe()
+    want = op.plan(case, sms)
+    for key in ("family", "chunk", "tokens_per_tile", "num_ctas", "max_chunks"):
+        assert got[key] == want[key], key
+    for key in ("items", "work_indptr", "nch_token", "merge_tokens"):
+        assert np.array_equal(got[key], want[key]), key
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
+def test_planner_matches_oracle_on_workloads(pa, n):
+    case = synth.config(n) if n != 3 and n != 5 else _light(n)
+    got = _plan(pa, case, 152).describe()
+    want = op.plan(case, 152)
+    for key in ("family", "chunk", "num_ctas", "max_chunks"):
+        assert got[key] == want[key], key
+    for key in ("items", "work_indptr", "nch_token", "merge_tokens"):
+        assert np.array_equal(got[key], want[key]), key
+
+
+def _light(n):
+    """Workloads 3 / 5 with their lengths and shapes but a tiny stand-in cache
+    (the planner only reads lengths)."""
+    full = {3: dict(q_heads=32, kv_heads=8, kv_dtype="int8", chunk_size=0),
+            5: dict(q_heads=128, kv_heads=1, head_dim_qk=576, head_dim_v=512, kv_dtype="int8",
+                    scale_kind="global", layout="mla", chunk_size=-1)}[n]
+    from synth.cases import _draw_lens, S_LEN_Q, S_LEN_KV
+    if n == 3:
+        ql, kv = _draw_lens(3, S_LEN_Q, 8, 64, 512), _draw_lens(3, S_LEN_KV, 8, 0, 8192)
+    else:
+        ql, kv = _draw_lens(5, S_LEN_Q, 32, 1, 2), _draw_lens(5, S_LEN_KV, 32, 4096, 16384)
+    return synth.make_case(name=f"light{n}", seed=n, seq_lens=ql, seq_lens_kv=kv, **full)
+
+
+def test_workspace_and_work_counts(pa):
+    case = synth.config(2)
+    d = _plan(pa, case).describe()
+    assert d["family"] == "decode" and d["chunk"] == 512
+    assert d["kv_bytes"] == case.kv_bytes_total()
+    T, H = case.total_q, case.q_heads
+    assert d["workspace_bytes"] >= T * d["max_chunks"] * H * (128 * 2 + 8)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("chunk_size", 100, 1),        # not a multiple of the page size
+    ("q_heads", 30, 1),            # not a multiple of kv_heads
+    ("head_dim_qk", 64, 2),        # no kernel built for it
+    ("sm_scale", -1.0, 1),
+    ("q_stride", 12, 1),
+])
+def test_invalid_problems_rejected(pa, field, value, status):
+    case = synth.make_case(name="v", seed=1, seq_lens=[2], seq_lens_kv=[10], q_heads=8,
+                           kv_heads=2, chunk_size=0)
+    prob = pa.problem_of(case)
+    setattr(prob, field, value)
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_plan(prob, case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, 152)
+    assert e.value.status == status
+
+
+def test_invalid_lengths_rejected(pa):
+    case = synth.make_case(name="v", seed=1, seq_lens=[2, 3], seq_lens_kv=[10, 5], q_heads=8,
+                           kv_heads=2, chunk_size=0)
+    prob = pa.problem_of(case)
+    with pytest.raises(pa.PaError):
+        pa.pa_plan(prob, [2, -1], case.seq_lens_kv, [0, 2, 1], 152)
+    with pytest.raises(pa.PaError):
+        pa.pa_plan(prob, case.seq_lens, case.seq_lens_kv, [0, 2, 4], 152)   # not a prefix sum
+    with pytest.raises(pa.PaError):
+        pa.pa_plan(prob, case.seq_lens, [10, 10_000], case.cu_seqlens_q, 152)  # too many pages
+
+
+def test_run_rejects_null_pointers_before_launch(pa):
+    case = synth.make_case(name="v", seed=1, seq_lens=[1], seq_lens_kv=[10], q_heads=8,
+                           kv_heads=2, chunk_size=0)
+    plan = _plan(pa, case)
+    args = pa.make_args(q=None, cache_k=None, cache_v=None, k_scale=None, v_scale=None,
+                        block_table=None, out=16)
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_run(plan, args, 256, None)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_run(plan, args, None, None)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    args2 = pa.make_args(q=16, cache_k=32, cache_v=64, k_scale=8, v_scale=8, block_table=8,
+                         out=8)
+    args2.q = 18   # misaligned
+    with pytest.raises(pa.PaError) as e:
+        pa.pa_run(plan, args2, 256, None)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
