@@ -25,7 +25,8 @@
  * Conventions for every entry point:
  *   - Device pointers are plain CUDA device addresses; host pointers are plain
  *     host addresses.  The library never allocates or frees device memory and
- *     never synchronises a stream except in pa_check.  All device work is
+ *     never synchronises a stream except in pa_check (and in pa_run_static
+ *     when asked to check).  All device work is
  *     enqueued on the caller's stream (a cudaStream_t passed as void*; NULL
  *     is the legacy default stream).
  *   - Every call returns a pa_status and never throws.  On failure the reason
@@ -193,6 +194,29 @@ pa_status pa_check(const pa_plan_t* plan, const void* workspace, void* stream, i
 void pa_plan_destroy(pa_plan_t* plan);
 
 const char* pa_last_error(void);
+
+/*
+ * pa_run_static: plan upload + pa_run + pa_merge in one call, using a
+ * workspace that lives inside the library instead of one the caller
+ * allocates.  (The source pages have no counterpart; this entry point exists
+ * for callers that cannot call cudaMalloc, such as a plugin whose host
+ * framework owns every device allocation, or a real-time loop where an
+ * allocation may block or fail.)  The caller still passes its inputs and
+ * outputs in args.
+ *   - The built-in buffer is a 32 MiB static device array, present on every
+ *     GPU where the library's kernels are loaded until the process exits.
+ *     Plans whose pa_workspace_size exceeds it return PA_ERR_INVALID_ARG
+ *     before any GPU work.
+ *   - No device memory is allocated or freed.  The first call on a device
+ *     looks up the buffer's device address (cudaGetSymbolAddress with that
+ *     device current); make that first call before any stream capture.
+ *   - All calls share the buffer, which keeps the last call's contents:
+ *     calls that may overlap on the GPU (other streams, other host threads)
+ *     race; serialise them.  The status word is cleared on every call.
+ *   - check != 0 synchronises the stream and returns the device status
+ *     (as pa_check would); check == 0 returns after enqueueing.
+ */
+pa_status pa_run_static(const pa_plan_t* plan, const pa_args* args, void* stream, int32_t check);
 
 /*
  * Test hook: copies the raw cache bytes of positions pos0 .. pos0+n-1 of

@@ -77,6 +77,7 @@ def _load():
         "pa_debug_gather": ([ctypes.POINTER(PaProblem), ctypes.POINTER(PaArgs), i32, i32, i32,
                              i32, vp, vp, vp], i32),
         "pa_debug_set_faults": ([i64, i32], i32),
+        "pa_run_static": ([vp, ctypes.POINTER(PaArgs), vp, i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -229,6 +230,13 @@ def pa_debug_gather(problem: PaProblem, args: PaArgs, b: int, kv_head: int, pos0
 
 def pa_debug_set_faults(wait_limit_ns: int = 0, skip_first_load: bool = False):
     _check(lib.pa_debug_set_faults(int(wait_limit_ns), int(bool(skip_first_load))))
+
+
+def pa_run_static(plan: Plan, args: PaArgs, stream=None, check: bool = False):
+    """Upload, run and merge with the library's built-in 32 MiB device workspace
+    (for callers that cannot allocate device memory; see include/pa.h).
+    check=True synchronises the stream and raises on a device-side error."""
+    _check(lib.pa_run_static(plan.handle, ctypes.byref(args), _stream(stream), int(bool(check))))
 
 
 def pa_last_error() -> str:
