@@ -238,6 +238,19 @@ pa_status pa_debug_gather(const pa_problem* problem, const pa_args* args, int32_
  */
 pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load);
 
+/*
+ * Timeline tracing (diagnostics).  With a non-null device buffer of
+ * ctas * tiles_per_cta * 16 uint64 entries, later pa_run calls record
+ * %globaltimer stamps (ns) of pipeline events: entry
+ * [(cta * tiles_per_cta + tile) * 16 + event] for the first `ctas` CTAs and
+ * their first `tiles_per_cta` KV tiles.  Events (decode kernel): 0 pages
+ * issued, 1/2 K dequantisation start/end, 3 scores ready, 4 P ready,
+ * 5/6 V dequantisation start/end, 7 V ready, 8 score MMA issued, 9 PV MMA
+ * issued, 10 item epilogue done, 11 P buffer free.  NULL disables tracing.
+ * Process-wide setting.
+ */
+pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta);
+
 #ifdef __cplusplus
 }
 #endif

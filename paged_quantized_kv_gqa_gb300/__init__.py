@@ -78,6 +78,7 @@ def _load():
                              i32, vp, vp, vp], i32),
         "pa_debug_set_faults": ([i64, i32], i32),
         "pa_run_static": ([vp, ctypes.POINTER(PaArgs), vp, i32], i32),
+        "pa_debug_set_trace": ([vp, i32, i32], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -237,6 +238,12 @@ def pa_run_static(plan: Plan, args: PaArgs, stream=None, check: bool = False):
     (for callers that cannot allocate device memory; see include/pa.h).
     check=True synchronises the stream and raises on a device-side error."""
     _check(lib.pa_run_static(plan.handle, ctypes.byref(args), _stream(stream), int(bool(check))))
+
+
+def pa_debug_set_trace(buf=None, ctas: int = 0, tiles_per_cta: int = 0):
+    """Enable (device uint64 buffer of ctas * tiles_per_cta * 16) or disable (None)
+    the kernels' %globaltimer pipeline trace."""
+    _check(lib.pa_debug_set_trace(_ptr(buf), int(ctas), int(tiles_per_cta)))
 
 
 def pa_last_error() -> str:

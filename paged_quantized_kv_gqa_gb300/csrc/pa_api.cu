@@ -27,7 +27,7 @@
 namespace pa {
 
 static thread_local std::string g_last_error;
-static FaultCfg g_faults{kDefaultWaitNs, 0};
+static FaultCfg g_faults{kDefaultWaitNs, 0, nullptr, 0, 0};
 static std::mutex g_fault_mu;
 
 void set_error(const std::string& msg) { g_last_error = msg; }
@@ -209,12 +209,15 @@ static pa_status build_plan(const pa_problem& prob, const int32_t* ql, const int
   for (int t = 0; t < P.total_q; ++t)
     if (P.nch_token[t] > 1) P.merge_tokens.push_back(t);
 
-  // device blob and workspace layout
+  // device blob and workspace layout; every array starts on a 16-byte boundary
+  // (the kernels read an item record as two 16-byte vectors)
+  auto align4 = [](size_t w) { return (w + 3) / 4 * 4; };
   P.off_indptr = 0;
-  P.off_items = P.off_indptr + P.work_indptr.size();
-  P.off_nch = P.off_items + P.items.size();
-  P.off_merge = P.off_nch + P.nch_token.size();
+  P.off_items = align4(P.off_indptr + P.work_indptr.size());
+  P.off_nch = align4(P.off_items + P.items.size());
+  P.off_merge = align4(P.off_nch + P.nch_token.size());
   const size_t words = P.off_merge + P.merge_tokens.size();
+  static_assert(kStatusBytes % 16 == 0, "plan blob must start 16-byte aligned");
   P.blob.assign(std::max<size_t>(words, 1), 0);
   std::copy(P.work_indptr.begin(), P.work_indptr.end(), P.blob.begin() + P.off_indptr);
   std::copy(P.items.begin(), P.items.end(), P.blob.begin() + P.off_items);
@@ -421,6 +424,9 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   p.scale_kind = pr.scale_kind;
   p.max_chunks = plan->max_chunks;
   p.skip_first_load = fc.skip_first_load;
+  p.trace = fc.trace;
+  p.trace_ctas = fc.trace_ctas;
+  p.trace_tiles = fc.trace_tiles;
   p.sm_scale_log2 = pr.sm_scale * 1.4426950408889634f;
 
   cudaError_t e;
@@ -495,6 +501,16 @@ pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load) {
   std::lock_guard<std::mutex> lk(g_fault_mu);
   g_faults.wait_limit_ns = wait_limit_ns == 0 ? kDefaultWaitNs : wait_limit_ns;
   g_faults.skip_first_load = skip_first_load ? 1 : 0;
+  return PA_OK;
+}
+
+pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta) {
+  if (device_buf && (ctas <= 0 || tiles_per_cta <= 0))
+    return fail(PA_ERR_INVALID_ARG, "trace buffer needs positive ctas and tiles_per_cta");
+  std::lock_guard<std::mutex> lk(g_fault_mu);
+  g_faults.trace = static_cast<uint64_t*>(device_buf);
+  g_faults.trace_ctas = device_buf ? ctas : 0;
+  g_faults.trace_tiles = device_buf ? tiles_per_cta : 0;
   return PA_OK;
 }
 

@@ -7,25 +7,34 @@
 // (token, head-in-group), chunk bounds [c*chunk, min(kv_len, (c+1)*chunk)),
 // direct write when the sequence has one chunk, else partial o plus tmp_m /
 // tmp_d).  The sm80 design there (cp.async + mma.sync with dequant in
-// registers) is replaced by:
+// registers, all warps doing every step) is replaced by:
 //
 //   * Swap-AB orientation.  The 128 TMEM lanes hold 128 KV positions, the
-//     packed query rows are the MMA's N (16..64).  S^T = K * Q'^T and
-//     O^T += V^T * P^T, so no query padding to M = 128 is needed.
-//   * A producer warp streams each (page, kv head) K slab [64 x 128] and V slab
-//     [128 x 64] with TMA (128B / 64B swizzle) into a 4-stage ring; a tile is
-//     two pages (128 positions).
-//   * The four math warps convert int8 / E4M3 bytes to fp16 (exact) and write
-//     them straight into TMEM as the A operand of tcgen05.mma (K rows on
-//     lanes = positions, V^T rows on lanes = head dims), so converted tiles
-//     never go back through shared memory.
-//   * Q' (bf16 query times the per-channel K scale, fp16) and P^T (fp16) are
-//     the B operands, K-major with 128B swizzle in shared memory.
-//   * Row sums are a second MMA, L += ones * P^T, accumulated in TMEM next to
-//     O; the running max is only raised when a tile exceeds it by more than
-//     2^8 (CTA-wide vote), and then O and L are rescaled in TMEM.
-//   * Per-kv-head / global K scales fold into the softmax scale, V scales
-//     into the epilogue; per-channel K scales fold into Q'.
+//     packed query rows are the MMA's N (16..64):  S^T = K * Q'^T and
+//     O^T += V^T * P^T, so queries are never padded to M = 128.
+//   * Warp specialisation, one persistent CTA of four warpgroups per SM:
+//       SM0, SM1  online softmax, each on half of the packed rows (lane =
+//                 position): running max (lazy, vote per half), row sums in
+//                 registers, P^T to shared memory, and the rare rescale of
+//                 its columns of O;
+//       CV        Q' of each item, K rows (lane = position) and V^T rows (lane
+//                 = head dim) dequantised straight into TMEM, and the epilogue;
+//       IO        one TMA warp ((page, kv head) K slab [64 x 128] with 128B
+//                 swizzle and V slab [128 x 64] with 64B swizzle per page) and
+//                 one MMA warp issuing S = K Q'^T and O += V^T P^T, polling
+//                 both queues and issuing whichever is ready.
+//     The roles meet only at mbarriers: K, V and S are double-buffered, P^T
+//     four-deep, Q' and O double-buffered per item (the epilogue of an item
+//     overlaps the next item), so dequantisation, softmax, tensor-core work
+//     and page loads of neighbouring tiles and items overlap.
+//   * tcgen05.mma with M = 128 costs about the same for any N <= 64, so the
+//     kernel issues the minimum: 8 MMAs for S and 8 for PV per 128-position
+//     tile; row sums are accumulated by the softmax warps.
+//   * Converted K / V never return to shared memory: they are the TMEM A
+//     operand.  Q' (bf16 query times the per-channel K scale, fp16) and P^T
+//     (fp16) are K-major 128B-swizzled shared-memory B operands.
+//   * Per-kv-head / global K scales fold into the softmax scale, V scales into
+//     the epilogue, per-channel K scales into Q'.
 #include <cfloat>
 
 #include "pa_internal.h"
@@ -35,32 +44,45 @@
 namespace pa {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kTileTok = 128;
 constexpr int kHeadDim = 128;
 constexpr int kPage = 64;
 constexpr int kSlab = kPage * kHeadDim;          // bytes of one (page, head) K or V slab
 constexpr int kStageBytes = 4 * kSlab;           // K (2 pages) + V (2 pages)
 constexpr float kTau = 8.0f;                     // lazy-rescale threshold (log2 units)
-constexpr int kMathThreads = 128;
-constexpr int kThreads = kMathThreads + 32;
+constexpr int kThreads = 512;                    // four warpgroups
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma = 13;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kPBufs = 4;                        // P^T ring depth
+constexpr int kItemRing = 8;                     // per-item row-sum / max hand-off ring
 
+constexpr int stages_for(int nr) { return nr <= 48 ? 4 : 3; }
+
+// TMEM columns: K[2] 0/64, V[2] 128/192, S[2] 256/256+NR, O[2] 256+2NR/256+3NR.
 template <int NR>
-struct Smem {
-  static constexpr int kQ = kStages * kStageBytes;
-  static constexpr int kP = kQ + NR * 256;
-  static constexpr int kRed = kP + 2 * NR * 256;
-  static constexpr int kBars = kRed + 4 * NR * 4;
-  static constexpr int kMisc = kBars + (2 * kStages + 2) * 8;
-  static constexpr int kTotal = kMisc + 16 + 1024;  // + alignment slack
+struct Tm {
+  static constexpr uint32_t K0 = 0, V0 = 128, S0 = 256, O0 = 256 + 2 * NR;
+  static_assert(256 + 4 * NR <= 512, "TMEM overflow");
 };
 
 template <int NR>
-struct Tm {
-  static constexpr uint32_t K = 0, V = 64, ONES = 128, S0 = 192, S1 = 192 + NR, O = 192 + 2 * NR,
-                            L = 192 + 3 * NR;
-  static constexpr uint32_t kUsed = 192 + 4 * NR;
-  static constexpr uint32_t kCols = kUsed <= 256 ? 256 : 512;
+struct Smem {
+  static constexpr int kStages = stages_for(NR);
+  static constexpr int kQ = kStages * kStageBytes;         // Q'[2]
+  static constexpr int kP = kQ + 2 * NR * 256;             // P^T ring
+  static constexpr int kRed = kP + kPBufs * NR * 256;      // [4][NR] warp maxima
+  static constexpr int kRedL = kRed + 4 * NR * 4;          // [4][NR] warp row sums
+  static constexpr int kLsum = kRedL + 4 * NR * 4;         // [ring][NR] item row sums
+  static constexpr int kMfin = kLsum + kItemRing * NR * 4; // [ring][NR] item running max
+  static constexpr int kM = kMfin + kItemRing * NR * 4;    // [NR] running max
+  static constexpr int kAlpha = kM + NR * 4;               // [NR] rescale factors
+  static constexpr int kBars = kAlpha + NR * 4;
+  // full[S], empty[S], kready[2], sfull[2], sfree[2], pready[4], vready[2], pvdone[4], lready[8]
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + kPBufs + 2 + kPBufs + kItemRing;
+  static constexpr int kMisc = kBars + kNumBars * 8;       // tmem addr, abort flags
+  static constexpr int kTotal = kMisc + 32 + 1024;         // + alignment slack
+  static_assert(kTotal <= 232448, "shared memory overflow");
 };
 
 __device__ __forceinline__ void record_status(int32_t* status, int code, int detail) {
@@ -70,15 +92,15 @@ __device__ __forceinline__ void record_status(int32_t* status, int code, int det
   }
 }
 
-// Waits on an mbarrier phase; gives up when the deadline passes or another
-// role has raised the CTA's abort flag.
+// Waits on an mbarrier phase; gives up at the deadline or once any role has
+// raised the CTA-wide abort flag.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int* abort_flag) {
+                                              volatile int* abort_any) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
+    if (*abort_any) return false;
     if (globaltimer() - t0 > limit_ns) return false;
   }
 }
@@ -87,6 +109,53 @@ __device__ __forceinline__ float load_scale(const void* s, int kind, int idx) {
   if (kind == PA_SCALE_GLOBAL) return reinterpret_cast<const float*>(s)[0];
   return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(s)[idx]);
 }
+
+struct Item {
+  int b, kvh, tok0, ntok, cbase, kv0, kv1, chunk, nch, ntiles;
+};
+
+__device__ __forceinline__ Item load_item(const int32_t* items, int it) {
+  const int4* r = reinterpret_cast<const int4*>(items + (int64_t)it * kItemWords);
+  const int4 a = r[0], c = r[1];
+  Item m;
+  m.b = a.x; m.kvh = a.y; m.tok0 = a.z; m.ntok = a.w;
+  m.cbase = c.x; m.kv0 = c.y; m.kv1 = c.z; m.chunk = c.w & 0xFFFF; m.nch = c.w >> 16;
+  m.ntiles = (m.kv1 - m.kv0 + kTileTok - 1) / kTileTok;
+  return m;
+}
+
+// %globaltimer stamp of pipeline event `ev` of tile g (diagnostic trace)
+__device__ __forceinline__ void trace_ev(const AttnParams& p, uint32_t g, int ev) {
+  if (p.trace != nullptr && (int)blockIdx.x < p.trace_ctas && (int)g < p.trace_tiles)
+    p.trace[((int64_t)blockIdx.x * p.trace_tiles + g) * 16 + ev] = globaltimer();
+}
+
+// lane-0 arrive after the whole warp finished its part
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+}
+
+// Walks the (item, tile) sequence of one CTA.
+struct TileCursor {
+  int it, end, i, ntiles;
+  const int32_t* items;
+  __device__ __forceinline__ void init(const int32_t* its, int begin, int e) {
+    items = its;
+    it = begin;
+    end = e;
+    i = 0;
+    ntiles = it < end ? load_item(items, it).ntiles : 0;
+  }
+  __device__ __forceinline__ bool valid() const { return it < end; }
+  __device__ __forceinline__ void advance() {
+    if (++i >= ntiles) {
+      ++it;
+      i = 0;
+      ntiles = it < end ? load_item(items, it).ntiles : 0;
+    }
+  }
+};
 
 }  // namespace
 
@@ -99,13 +168,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~uintptr_t(1023));
   using SM = Smem<NR>;
   using TM = Tm<NR>;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+  constexpr int kStages = SM::kStages;
+  constexpr int NH = NR / 2;       // rows per softmax warpgroup
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+  uint64_t* full = bars;
   uint64_t* empty = full + kStages;
-  uint64_t* bar_s = empty + kStages;
-  uint64_t* bar_pv = bar_s + 1;
+  uint64_t* kready = empty + kStages;
+  uint64_t* sfull = kready + 2;
+  uint64_t* sfree = sfull + 2;
+  uint64_t* pready = sfree + 2;
+  uint64_t* vready = pready + kPBufs;
+  uint64_t* pvdone = vready + 2;
+  uint64_t* lready = pvdone + kPBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
+  volatile int* abort_any = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
+  volatile int* abort_grp = reinterpret_cast<volatile int*>(smem + SM::kMisc + 8);  // [2]
   float* red = reinterpret_cast<float*>(smem + SM::kRed);
+  float* red_l = reinterpret_cast<float*>(smem + SM::kRedL);
+  float* lsum_s = reinterpret_cast<float*>(smem + SM::kLsum);
+  float* mfin_s = reinterpret_cast<float*>(smem + SM::kMfin);
+  float* m_s = reinterpret_cast<float*>(smem + SM::kM);
+  float* alpha_s = reinterpret_cast<float*>(smem + SM::kAlpha);
   const uint32_t s_base = smem_u32(smem);
   const uint32_t q_s = s_base + SM::kQ;
   const uint32_t p_s = s_base + SM::kP;
@@ -113,28 +196,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int wg = warp >> 2;         // warpgroup: 0, 1 softmax; 2 CV; 3 IO
   const int item_begin = p.work_indptr[blockIdx.x];
   const int item_end = p.work_indptr[blockIdx.x + 1];
   const uint64_t limit = (uint64_t)p.wait_limit_ns;
+  const int G = p.group;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 4);
     }
-    mbar_init(bar_s, 1);
-    mbar_init(bar_pv, 1);
-    *abort_flag = 0;
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&kready[j], 4);
+      mbar_init(&sfull[j], 1);
+      mbar_init(&sfree[j], 8);
+      mbar_init(&vready[j], 4);
+    }
+    for (int j = 0; j < kPBufs; ++j) {
+      mbar_init(&pready[j], 8);
+      mbar_init(&pvdone[j], 1);
+    }
+    for (int j = 0; j < kItemRing; ++j) mbar_init(&lready[j], 8);
+    *abort_any = 0;
+    abort_grp[0] = 0;
+    abort_grp[1] = 0;
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, TM::kCols);
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // this warp's TMEM lane quarter (a warp may only touch lanes 32*(warp%4) ..)
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
+  if (warp == kWarpTma) {
+    // ================================================================ TMA
     if (lane == 0) {
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
@@ -143,110 +241,321 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued_g[s] = -1;
       bool ok = true;
       for (int it = item_begin; it < item_end && ok; ++it) {
-        const int* rec = p.items + (int64_t)it * kItemWords;
-        const int b = rec[0], kvh = rec[1], kv0 = rec[5], kv1 = rec[6];
-        const int ntiles = (kv1 - kv0 + kTileTok - 1) / kTileTok;
-        for (int t = 0; t < ntiles; ++t, ++g) {
+        const Item m = load_item(p.items, it);
+        const int32_t* bt = p.block_table + (int64_t)m.b * p.max_blocks;
+        for (int t = 0; t < m.ntiles; ++t, ++g) {
           const int stage = g % kStages;
           const uint32_t ph = (g / kStages) & 1;
-          if (!wait_or_abort(&empty[stage], ph ^ 1, limit, abort_flag)) {
-            // only the math warps write the abort flag (they read it right after
-            // their own barriers); the loader just records the timeout and stops
-            if (!*abort_flag) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+          const int pos0 = m.kv0 + t * kTileTok;
+          const int npg = (m.kv1 - pos0) > kPage ? 2 : 1;
+          // the page ids are read before waiting so their latency overlaps the wait
+          int pages[2];
+          pages[0] = bt[pos0 / kPage];
+          pages[1] = npg == 2 ? bt[pos0 / kPage + 1] : 0;
+          if (!wait_or_abort(&empty[stage], ph ^ 1, limit, abort_any)) {
+            if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+            *abort_any = 1;
             ok = false;
             break;
           }
-          const int pos0 = kv0 + t * kTileTok;
-          const int npg = (kv1 - pos0) > kPage ? 2 : 1;
           if (p.skip_first_load && g == 0) continue;  // failure-detection test hook
           mbar_arrive_expect_tx(&full[stage], (uint32_t)(npg * 2 * kSlab));
           issued_g[stage] = (int)g;
           uint8_t* st = smem + stage * kStageBytes;
           for (int pg = 0; pg < npg; ++pg) {
-            const int page = page_of(p.block_table, p.max_blocks, b, pos0 + pg * kPage, kPage);
+            const int page = pages[pg];
             int yk, yv;
             if (page < 0 || page >= p.num_pages) {
               record_status(p.status, PA_ERR_BAD_PAGE, it);
               yk = p.num_pages * p.kv_heads * kPage;       // past the end: TMA fills zeros
               yv = p.num_pages * p.kv_heads * kHeadDim;
             } else {
-              yk = (page * p.kv_heads + kvh) * kPage;
-              yv = (page * p.kv_heads + kvh) * kHeadDim;
+              yk = (page * p.kv_heads + m.kvh) * kPage;
+              yv = (page * p.kv_heads + m.kvh) * kHeadDim;
             }
             tma_load_2d(st + pg * kSlab, &tm_k, &full[stage], 0, yk);
             tma_load_2d(st + 2 * kSlab + pg * kSlab, &tm_v, &full[stage], 0, yv);
           }
+          trace_ev(p, g, 0);
         }
       }
-      // drain: every load still in flight lands before the CTA may exit
-      for (int s = 0; s < kStages; ++s) {
+      for (int s = 0; s < kStages; ++s)   // every issued load lands before exit
         if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, limit);
+    }
+  } else if (warp == kWarpMma) {
+    // ================================================================ MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(128, NR);
+      TileCursor cs, cp;       // next S to issue, next PV to issue
+      cs.init(p.items, item_begin, item_end);
+      cp.init(p.items, item_begin, item_end);
+      uint32_t gs = 0, gp = 0;
+      uint32_t s_commits[2] = {0, 0}, pv_commits[kPBufs] = {0, 0, 0, 0};
+      bool ok = true;
+      uint64_t t_idle = 0;
+      while (cp.valid()) {
+        bool progressed = false;
+        if (cs.valid() && mbar_try_wait(&kready[gs & 1], (gs >> 1) & 1) &&
+            (gs < 2 || mbar_try_wait(&sfree[gs & 1], ((gs - 2) >> 1) & 1))) {
+          tc_fence_after();
+          const uint32_t kb = TM::K0 + (gs & 1) * 64;
+          const uint32_t sd = TM::S0 + (gs & 1) * NR;
+          const uint32_t qb = q_s + ((cs.it - item_begin) & 1) * NR * 256;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + sd, tmem + kb + 8 * kk,
+                   sdesc_k128(qb + (kk >> 2) * NR * 128 + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
+          tc_commit(&sfull[gs & 1]);
+          ++s_commits[gs & 1];
+          trace_ev(p, gs, 8);
+          ++gs;
+          cs.advance();
+          progressed = true;
+        }
+        if (gp < gs && mbar_try_wait(&pready[gp & 3], (gp >> 2) & 1) &&
+            mbar_try_wait(&vready[gp & 1], (gp >> 1) & 1)) {
+          tc_fence_after();
+          const uint32_t vb = TM::V0 + (gp & 1) * 64;
+          const uint32_t pb = p_s + (gp & 3) * NR * 256;
+          const uint32_t od = TM::O0 + ((cp.it - item_begin) & 1) * NR;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bd = sdesc_k128(pb + (kk >> 2) * NR * 128 + (kk & 3) * 32);
+            mma_ts(tmem + od, tmem + vb + 8 * kk, bd, idesc, (cp.i > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&pvdone[gp & 3]);
+          ++pv_commits[gp & 3];
+          trace_ev(p, gp, 9);
+          ++gp;
+          cp.advance();
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          if (*abort_any) { ok = false; break; }
+          const uint64_t now = globaltimer();
+          if (t_idle == 0) t_idle = now;
+          else if (now - t_idle > limit) { ok = false; break; }
+        }
+      }
+      if (!ok) {
+        if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
+        *abort_any = 1;
+      }
+      // drain: every issued MMA completes before TMEM is released
+      for (int j = 0; j < 2; ++j)
+        if (s_commits[j]) mbar_wait(&sfull[j], (s_commits[j] - 1) & 1, limit);
+      for (int j = 0; j < kPBufs; ++j)
+        if (pv_commits[j]) mbar_wait(&pvdone[j], (pv_commits[j] - 1) & 1, limit);
+    }
+  } else if (wg == 3) {
+    // warps 14-15: no role (they complete the fourth warpgroup)
+  } else if (wg < 2) {
+    // ================================================================ softmax
+    // warpgroup wg owns packed rows [r_lo, r_lo + NH); lane = position
+    const int r_lo = wg * NH;
+    const int bar_id = 1 + wg;
+    const int pos_in_tile = tid & 127;
+    volatile int* my_abort = abort_grp + wg;
+    bool fail = false, stop = false;
+    auto note_fail = [&](int it) {
+      if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+      *abort_any = 1;
+      *my_abort = 1;
+      fail = true;
+    };
+    uint32_t g = 0;
+    float l[NH];
+    for (int it = item_begin; it < item_end && !stop; ++it) {
+      const Item cur = load_item(p.items, it);
+      const int li = it - item_begin;
+      const int n_rows = cur.ntok * G;
+      const float c_log2 = p.sm_scale_log2 *
+          (p.scale_kind == PA_SCALE_PER_CHANNEL ? 1.0f : load_scale(p.k_scale, p.scale_kind, cur.kvh));
+      const uint32_t o_col = TM::O0 + (li & 1) * NR + r_lo;
+#pragma unroll
+      for (int j = 0; j < NH; ++j) l[j] = 0.0f;
+      for (int i = 0; i < cur.ntiles; ++i, ++g) {
+        // ---- S_g columns of this half -> registers, then release the S buffer
+        float s[NH];
+        if (!fail && !wait_or_abort(&sfull[g & 1], (g >> 1) & 1, limit, abort_any)) note_fail(it);
+        tc_fence_after();
+        if (tid == 0) trace_ev(p, g, 3);
+        if (!fail) {
+#pragma unroll
+          for (int c = 0; c < NH / 8; ++c) {
+            uint32_t v[8];
+            tmem_ld8(t_lane + TM::S0 + (g & 1) * NR + r_lo + 8 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s[8 * c + j] = __uint_as_float(v[j]);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NH; ++j) s[j] = 0.f;
+        }
+        tc_fence_before();
+        warp_arrive(&sfree[g & 1], lane);
+
+        // ---- x = s * c (log2 units), -inf where masked
+        const int tpos0 = cur.kv0 + i * kTileTok;
+        const int jpos = tpos0 + pos_in_tile;
+        const bool need_mask = (tpos0 + kTileTok > cur.kv1) || (tpos0 + kTileTok - 1 > cur.cbase);
+        if (need_mask) {
+          const int lim_tok = jpos - cur.cbase;   // visible for rows of token >= lim_tok
+#pragma unroll
+          for (int j = 0; j < NH; ++j) {
+            const bool vis = (jpos < cur.kv1) && (r_lo + j >= lim_tok * G);
+            s[j] = vis ? s[j] * c_log2 : -INFINITY;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < NH; ++j) s[j] *= c_log2;
+        }
+        // the first tile of an item always sets the running max
+        bool exceed = (i == 0);
+        if (i > 0) {
+#pragma unroll
+          for (int j = 0; j < NH; ++j)
+            if (r_lo + j < n_rows) exceed |= (s[j] - m_s[r_lo + j] > kTau);
+        }
+        const bool resc = bar_or(bar_id, 128, exceed);
+        if (*my_abort) { fail = true; stop = true; break; }
+        if (resc) {
+          // exact tile maximum per row, new running max; rescale l (registers)
+          // and this half's columns of O (TMEM) by 2^(m_old - m_new)
+#pragma unroll
+          for (int j = 0; j < NH; ++j) {
+            const float wm = warp_max(s[j]);
+            if (lane == 0) red[(warp & 3) * NR + r_lo + j] = wm;
+          }
+          bar_sync(bar_id, 128);
+          if (pos_in_tile < NH) {
+            const int r = r_lo + pos_in_tile;
+            float a = 1.0f, mn = 0.0f;   // padded rows keep m = 0
+            if (r < n_rows) {
+              const float mo = (i == 0) ? -INFINITY : m_s[r];
+              const float tm = fmaxf(fmaxf(red[r], red[NR + r]), fmaxf(red[2 * NR + r], red[3 * NR + r]));
+              mn = fmaxf(mo, tm);
+              a = (mo == -INFINITY) ? 0.0f : fast_exp2(mo - mn);
+            }
+            m_s[r] = mn;
+            alpha_s[r] = a;
+          }
+          bar_sync(bar_id, 128);
+#pragma unroll
+          for (int j = 0; j < NH; ++j) l[j] *= alpha_s[r_lo + j];
+          if (i > 0) {
+            // O holds PV of the earlier tiles of this item: wait for the last one
+            if (!fail && !wait_or_abort(&pvdone[(g - 1) & 3], ((g - 1) >> 2) & 1, limit, abort_any))
+              note_fail(it);
+            tc_fence_after();
+            if (!fail) {
+#pragma unroll
+              for (int c = 0; c < NH / 8; ++c) {
+                uint32_t v[8];
+                tmem_ld8(t_lane + o_col + 8 * c, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha_s[r_lo + 8 * c + j]);
+                tmem_st8(t_lane + o_col + 8 * c, v);
+              }
+              tmem_wait_st();
+            }
+          }
+          bar_sync(bar_id, 128);  // red / alpha_s are reused by the next rescale
+        }
+        // P^T slot g&3 was last read by PV_{g-4}
+        if (g >= kPBufs && !fail &&
+            !wait_or_abort(&pvdone[g & 3], ((g - kPBufs) >> 2) & 1, limit, abort_any))
+          note_fail(it);
+        if (tid == 0) trace_ev(p, g, 11);
+        {
+          // even lanes store row r, odd lanes row r + 4 (disjoint bank groups)
+          uint32_t* pw = reinterpret_cast<uint32_t*>(smem + SM::kP + (g & 3) * NR * 256);
+          const bool odd = lane & 1;
+          const int tt = pos_in_tile & ~1;
+          const int base = (tt >> 6) * NR * 128 + ((tt & 7) * 2);
+          const int chunk16 = (tt & 63) >> 3;
+#pragma unroll
+          for (int j0 = 0; j0 < NH; j0 += 8) {
+            float mr[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mr[k] = m_s[r_lo + j0 + k];
+#pragma unroll
+            for (int j1 = 0; j1 < 4; ++j1) {
+              const int j = j0 + j1;
+              const float p0 = s[j] == -INFINITY ? 0.f : fast_exp2(s[j] - mr[j1]);
+              const float p1 = s[j + 4] == -INFINITY ? 0.f : fast_exp2(s[j + 4] - mr[j1 + 4]);
+              l[j] += p0;
+              l[j + 4] += p1;
+              const float recv = __shfl_xor_sync(0xffffffffu, odd ? p0 : p1, 1);
+              const int rr = r_lo + (odd ? j + 4 : j);
+              const uint32_t word = odd ? pack_half2(recv, p1) : pack_half2(p0, recv);
+              pw[(base + rr * 128 + ((chunk16 ^ (rr & 7)) << 4)) >> 2] = word;
+            }
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        warp_arrive(&pready[g & 3], lane);
+        if (tid == 0) trace_ev(p, g, 4);
+        if (i + 1 == cur.ntiles) {
+          // row sums over all positions of the item: warp, then warpgroup
+#pragma unroll
+          for (int j = 0; j < NH; ++j) {
+            float v = l[j];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) red_l[(warp & 3) * NR + r_lo + j] = v;
+          }
+          bar_sync(bar_id, 128);
+          const int slot = li & (kItemRing - 1);
+          if (pos_in_tile < NH) {
+            const int r = r_lo + pos_in_tile;
+            lsum_s[slot * NR + r] = red_l[r] + red_l[NR + r] + red_l[2 * NR + r] + red_l[3 * NR + r];
+            mfin_s[slot * NR + r] = m_s[r];
+          }
+          warp_arrive(&lready[slot], lane);
+        }
       }
     }
   } else {
-    // ------------------------------------------------------------ math warps
-    const uint32_t t_lane = tmem + ((uint32_t)(warp * 32) << 16);
-    {
-      uint32_t ones[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) ones[j] = 0x3C003C00u;  // fp16 1.0, 1.0
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st16(t_lane + TM::ONES + 16 * c, ones);
-      tmem_wait_st();
-    }
-    const uint32_t idesc = idesc_f16_f32(128, NR);
-    const int G = p.group;
+    // ================================================================ CV warpgroup
+    // Q' of each item, K rows (lane = position) and V^T rows (lane = head dim)
+    // into TMEM, and the epilogue of each item (deferred by one item)
+    const int d = tid & 127;  // TMEM lane: K position / V head dim / output dim
     uint32_t g = 0;
-    uint32_t s_issued = 0, s_waited = 0, pv_issued = 0, pv_waited = 0;
     bool fail = false;
-
-    auto wait_s_upto = [&](uint32_t k) -> bool {
-      while (s_waited < k) {
-        if (!wait_or_abort(bar_s, s_waited & 1, limit, abort_flag)) return false;
-        ++s_waited;
-      }
-      return true;
-    };
-    auto wait_pv_upto = [&](uint32_t k) -> bool {
-      while (pv_waited < k) {
-        if (!wait_or_abort(bar_pv, pv_waited & 1, limit, abort_flag)) return false;
-        ++pv_waited;
-      }
-      return true;
-    };
     auto note_fail = [&](int it) {
-      if (!*abort_flag) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
-      *abort_flag = 1;
+      if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+      *abort_any = 1;
       fail = true;
     };
-
-    for (int it = item_begin; it < item_end; ++it) {
-      const int* rec = p.items + (int64_t)it * kItemWords;
-      const int kvh = rec[1], tok0 = rec[2], ntok = rec[3], cbase = rec[4];
-      const int kv0 = rec[5], kv1 = rec[6];
-      const int chunk = rec[7] & 0xFFFF, nch = rec[7] >> 16;
-      const int n_rows = ntok * G;
-      const int ntiles = (kv1 - kv0 + kTileTok - 1) / kTileTok;
-      const float c_log2 =
-          p.sm_scale_log2 *
-          (p.scale_kind == PA_SCALE_PER_CHANNEL ? 1.0f : load_scale(p.k_scale, p.scale_kind, kvh));
-
-      // ---- Q' -> shared memory (fp16, K-major, 128B swizzle, rows >= n_rows zero)
-      for (int task = tid; task < NR * 16; task += kMathThreads) {
+    // Q' of an item -> shared memory buffer qb (fp16, K-major, 128B swizzle, padded rows zero)
+    auto load_q = [&](const Item& m, uint32_t qb) {
+      const int n_rows = m.ntok * G;
+      for (int task = d; task < NR * 16; task += 128) {
         const int r = task >> 4, ch = task & 15;
         uint4 packed = make_uint4(0, 0, 0, 0);
         if (r < n_rows) {
-          const int token = tok0 + r / G;
-          const int head = kvh * G + r % G;
+          const int token = m.tok0 + r / G;
+          const int head = m.kvh * G + r % G;
           const uint4 raw = *reinterpret_cast<const uint4*>(p.q + (int64_t)token * p.q_stride +
                                                             head * kHeadDim + ch * 8);
           const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
           float f[8];
+          if (p.scale_kind == PA_SCALE_PER_CHANNEL) {
+            const uint4 sr = *reinterpret_cast<const uint4*>(
+                reinterpret_cast<const __nv_bfloat16*>(p.k_scale) + m.kvh * kHeadDim + ch * 8);
+            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(&sr);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            f[e] = __bfloat162float(hv[e]);
-            if (p.scale_kind == PA_SCALE_PER_CHANNEL)
-              f[e] *= load_scale(p.k_scale, PA_SCALE_PER_CHANNEL, kvh * kHeadDim + ch * 8 + e);
+            for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]) * __bfloat162float(sv[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]);
           }
           packed.x = pack_half2(f[0], f[1]);
           packed.y = pack_half2(f[2], f[3]);
@@ -254,179 +563,135 @@ __global__ void __launch_bounds__(kThreads, 1)
           packed.w = pack_half2(f[6], f[7]);
         }
         const int kb = ch >> 3, cc = ch & 7;
-        st_shared_v4(q_s + kb * NR * 128 + r * 128 + ((cc ^ (r & 7)) << 4), packed);
+        st_shared_v4(qb + kb * NR * 128 + r * 128 + ((cc ^ (r & 7)) << 4), packed);
       }
       fence_proxy_async_smem();
-
-      float m[NR];
+    };
+    // epilogue of local item li (tiles ending at global tile gl): O / row sum
+    auto epilogue = [&](int li, uint32_t gl) -> bool {
+      const int it = item_begin + li;
+      const Item m = load_item(p.items, it);
+      const int slot = li & (kItemRing - 1);
+      if (!wait_or_abort(&lready[slot], (li / kItemRing) & 1, limit, abort_any) ||
+          !wait_or_abort(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
+        note_fail(it);
+        return false;
+      }
+      tc_fence_after();
+      float o[NR];
+      const uint32_t ob = TM::O0 + (li & 1) * NR;
 #pragma unroll
-      for (int r = 0; r < NR; ++r) m[r] = (r < n_rows) ? -INFINITY : 0.0f;
-      bool first_pv = true;
-      const uint32_t s_item = s_issued, pv_item = pv_issued;
-
-      for (int i = 0; i <= ntiles && !fail; ++i) {
-        // ---------------- K of tile i -> TMEM, issue S_i = K_i * Q'^T
-        if (i < ntiles) {
-          if (!wait_s_upto(s_item + i)) { note_fail(it); }
-          const int stage = g % kStages;
-          const uint32_t ph = (g / kStages) & 1;
-          if (!fail && !wait_or_abort(&full[stage], ph, limit, abort_flag)) note_fail(it);
-          if (!fail) {
-            const int box = tid >> 6, row = tid & 63;
-            const uint32_t kbase = s_base + stage * kStageBytes + box * kSlab + row * 128;
+      for (int c = 0; c < NR / 16; ++c) {
+        uint32_t v[16];
+        tmem_ld16(t_lane + ob + 16 * c, v);
+        tmem_wait_ld();
 #pragma unroll
-            for (int c2 = 0; c2 < 4; ++c2) {
-              uint32_t w[16];
+        for (int j = 0; j < 16; ++j) o[16 * c + j] = __uint_as_float(v[j]);
+      }
+      tc_fence_before();
+      const float* mf = mfin_s + slot * NR;
+      const float* ls = lsum_s + slot * NR;
+      const int n_rows = m.ntok * G;
+      const float vs = load_scale(p.v_scale, p.scale_kind,
+                                  p.scale_kind == PA_SCALE_PER_CHANNEL ? m.kvh * kHeadDim + d : m.kvh);
+      const float ln2 = 0.69314718055994530942f;
+      int token = m.tok0, gq = 0;   // row r <-> (token, head-in-group gq)
 #pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const int c = c2 * 2 + h;
-                const uint4 raw = ld_shared_v4(kbase + ((c ^ (row & 7)) << 4));
-                cvt4<FP8>(raw.x, w[8 * h + 0], w[8 * h + 1]);
-                cvt4<FP8>(raw.y, w[8 * h + 2], w[8 * h + 3]);
-                cvt4<FP8>(raw.z, w[8 * h + 4], w[8 * h + 5]);
-                cvt4<FP8>(raw.w, w[8 * h + 6], w[8 * h + 7]);
-              }
-              tmem_st16(t_lane + TM::K + 16 * c2, w);
-            }
-            tmem_wait_st();
-          }
-          tc_fence_before();
-          bar_sync(1, kMathThreads);
-          if (*abort_flag) { fail = true; break; }
-          if (tid == 0) {
-            tc_fence_after();
-            const uint32_t sb = (i & 1) ? TM::S1 : TM::S0;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bd = sdesc_k128(q_s + (kk >> 2) * NR * 128 + (kk & 3) * 32);
-              mma_ts(tmem + sb, tmem + TM::K + 8 * kk, bd, idesc, kk > 0 ? 1u : 0u);
-            }
-            tc_commit(bar_s);
-          }
-          ++s_issued;
-          ++g;
-        }
-        if (i == 0) continue;
-
-        // ---------------- softmax of tile i-1
-        const int tl = i - 1;
-        const int stage_prev = (g - 1 - (i < ntiles ? 1 : 0)) % kStages;
-        if (!wait_s_upto(s_item + i)) { note_fail(it); }
-        tc_fence_after();
-        float s[NR];
-        if (!fail) {
-          const uint32_t sb = (tl & 1) ? TM::S1 : TM::S0;
-#pragma unroll
-          for (int c = 0; c < NR / 16; ++c) {
-            uint32_t v[16];
-            tmem_ld16(t_lane + sb + 16 * c, v);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 16; ++j) s[16 * c + j] = __uint_as_float(v[j]);
-          }
-        } else {
-#pragma unroll
-          for (int r = 0; r < NR; ++r) s[r] = 0.f;
-        }
-        const int tpos0 = kv0 + tl * kTileTok;
-        const int jpos = tpos0 + tid;
-        const bool need_mask = (tpos0 + kTileTok > kv1) || (tpos0 + kTileTok - 1 > cbase);
-        float t[NR];
-        bool exceed = false;
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-          bool vis = true;
-          if (need_mask) vis = (jpos < kv1) && (jpos <= cbase + r / G);
-          t[r] = vis ? fmaf(s[r], c_log2, -m[r]) : -INFINITY;
-          if (r < n_rows) exceed |= (t[r] > kTau);
-        }
-        const bool resc = bar_or(1, kMathThreads, exceed);
-        if (*abort_flag) { fail = true; break; }
-        if (resc) {
-          // exact tile maximum per row, new running max, rescale O and L
-#pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            const float x = (t[r] == -INFINITY) ? -INFINITY : s[r] * c_log2;
-            const float wm = warp_max(x);
-            if (lane == 0) red[warp * NR + r] = wm;
-          }
-          bar_sync(1, kMathThreads);
-          float alpha[NR];
-#pragma unroll
-          for (int r = 0; r < NR; ++r) {
-            alpha[r] = 1.0f;
-            if (r < n_rows) {
-              const float tm = fmaxf(fmaxf(red[r], red[NR + r]), fmaxf(red[2 * NR + r], red[3 * NR + r]));
-              const float mn = fmaxf(m[r], tm);
-              alpha[r] = (m[r] == -INFINITY) ? 0.0f : fast_exp2(m[r] - mn);
-              m[r] = mn;
+      for (int r = 0; r < NR; ++r) {
+        if (r < n_rows) {
+          const int head = m.kvh * G + gq;
+          const float lr = ls[r];
+          const float inv = lr > 0.f ? 1.0f / lr : 0.f;
+          const __nv_bfloat16 val = __float2bfloat16_rn(o[r] * inv * vs);
+          if (m.nch == 1) {
+            p.out[((int64_t)token * p.q_heads + head) * kHeadDim + d] = val;
+            if (d == r && p.lse != nullptr)
+              p.lse[(int64_t)token * p.q_heads + head] =
+                  lr > 0.f ? (mf[r] + __log2f(lr)) * ln2 : -INFINITY;
+          } else {
+            const int64_t slot_p = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
+            p.part_o[slot_p * kHeadDim + d] = val;
+            if (d == r) {
+              p.part_m[slot_p] = lr > 0.f ? mf[r] * ln2 : -INFINITY;
+              p.part_d[slot_p] = lr;
             }
           }
-          if (!first_pv) {
-            if (!wait_pv_upto(pv_item + tl)) { note_fail(it); }
-            tc_fence_after();
-            if (!fail) {
-#pragma unroll
-              for (int acc = 0; acc < 2; ++acc) {
-                const uint32_t base = acc == 0 ? TM::O : TM::L;
-#pragma unroll
-                for (int c = 0; c < NR / 16; ++c) {
-                  uint32_t v[16];
-                  tmem_ld16(t_lane + base + 16 * c, v);
-                  tmem_wait_ld();
-#pragma unroll
-                  for (int j = 0; j < 16; ++j)
-                    v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[16 * c + j]);
-                  tmem_st16(t_lane + base + 16 * c, v);
-                }
-              }
-              tmem_wait_st();
-            }
-          }
-#pragma unroll
-          for (int r = 0; r < NR; ++r)
-            t[r] = (t[r] == -INFINITY) ? -INFINITY : fmaf(s[r], c_log2, -m[r]);
         }
-        // P^T (fp16) -> shared memory, B operand [NR rows][128 positions], K-major SW128
+        if (++gq == G) {
+          gq = 0;
+          ++token;
+        }
+      }
+      if (d == 0) trace_ev(p, gl, 10);
+      return true;
+    };
+    uint32_t g_last_prev = 0;   // last tile of the previous item
+    for (int it = item_begin; it < item_end && !fail; ++it) {
+      const Item m = load_item(p.items, it);
+      const int li = it - item_begin;
+      for (int i = 0; i < m.ntiles; ++i, ++g) {
+        const int stage = g % kStages;
+        // K buffer g&1 was last read by S_{g-2}; Q' buffer li&1 by the S of item
+        // li-2, whose last tile is at most g-2
+        if (g >= 2 && !wait_or_abort(&sfull[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
+          note_fail(it);
+          break;
+        }
+        if (i == 0) load_q(m, q_s + (li & 1) * NR * 256);
+        if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
+        if (d == 0) trace_ev(p, g, 1);
         {
-          const uint32_t pbuf = p_s + (tl & 1) * NR * 256;
-          const bool odd = lane & 1;
-          const int tt = tid & ~1;
-          const int kb = tt >> 6;
-          const int chunk16 = (tt & 63) >> 3;
-          const int within = (tt & 7) * 2;
+          const int box = d >> 6, row = d & 63;
+          const uint32_t kbase = s_base + stage * kStageBytes + box * kSlab + row * 128;
+          uint4 raw[8];
 #pragma unroll
-          for (int r = 0; r < NR; r += 2) {
-            const float p0 = fast_exp2(t[r]);
-            const float p1 = fast_exp2(t[r + 1]);
-            const float send = odd ? p0 : p1;
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
-            const int rr = odd ? r + 1 : r;
-            const uint32_t word = odd ? pack_half2(recv, p1) : pack_half2(p0, recv);
-            st_shared_u32(pbuf + kb * NR * 128 + rr * 128 + ((chunk16 ^ (rr & 7)) << 4) + within,
-                          word);
+          for (int c = 0; c < 8; ++c) raw[c] = ld_shared_v4(kbase + ((c ^ (row & 7)) << 4));
+          const uint32_t dst = t_lane + TM::K0 + (g & 1) * 64;
+#pragma unroll
+          for (int c2 = 0; c2 < 4; ++c2) {
+            uint32_t w[16];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 r4 = raw[c2 * 2 + h];
+              cvt4<FP8>(r4.x, w[8 * h + 0], w[8 * h + 1]);
+              cvt4<FP8>(r4.y, w[8 * h + 2], w[8 * h + 3]);
+              cvt4<FP8>(r4.z, w[8 * h + 4], w[8 * h + 5]);
+              cvt4<FP8>(r4.w, w[8 * h + 6], w[8 * h + 7]);
+            }
+            tmem_st16(dst + 16 * c2, w);
           }
-          fence_proxy_async_smem();
+          tmem_wait_st();
         }
-
-        // ---------------- V of tile i-1 -> TMEM, issue PV_{i-1} and L_{i-1}
-        if (!wait_pv_upto(pv_item + tl)) { note_fail(it); }
+        tc_fence_before();
+        warp_arrive(&kready[g & 1], lane);
+        if (d == 0) trace_ev(p, g, 2);
+        // V buffer g&1 was last read by PV_{g-2}
+        if (g >= 2 && !wait_or_abort(&pvdone[(g - 2) & 3], ((g - 2) >> 2) & 1, limit, abort_any)) {
+          note_fail(it);
+          break;
+        }
         tc_fence_after();
-        if (!fail) {
-          const int nvalid = min(kTileTok, kv1 - tpos0);
-          const int d = tid;
-          const uint32_t vbase = s_base + stage_prev * kStageBytes + 2 * kSlab;
+        if (d == 0) trace_ev(p, g, 5);
+        {
+          // V^T row d of tile g -> TMEM V buffer g&1 (positions past kv1 zeroed)
+          const int tpos0 = m.kv0 + i * kTileTok;
+          const int nvalid = min(kTileTok, m.kv1 - tpos0);
+          const uint32_t vbase = s_base + stage * kStageBytes + 2 * kSlab + d * 64;
+          uint4 raw[8];
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            raw[c] = ld_shared_v4(vbase + (c >> 2) * kSlab + (((c & 3) ^ ((d >> 1) & 3)) << 4));
+          const uint32_t dst = t_lane + TM::V0 + (g & 1) * 64;
 #pragma unroll
           for (int box = 0; box < 2; ++box) {
             uint32_t w[32];
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-              const uint4 raw =
-                  ld_shared_v4(vbase + box * kSlab + d * 64 + ((c ^ ((d >> 1) & 3)) << 4));
-              cvt4<FP8>(raw.x, w[8 * c + 0], w[8 * c + 1]);
-              cvt4<FP8>(raw.y, w[8 * c + 2], w[8 * c + 3]);
-              cvt4<FP8>(raw.z, w[8 * c + 4], w[8 * c + 5]);
-              cvt4<FP8>(raw.w, w[8 * c + 6], w[8 * c + 7]);
+              const uint4 r4 = raw[box * 4 + c];
+              cvt4<FP8>(r4.x, w[8 * c + 0], w[8 * c + 1]);
+              cvt4<FP8>(r4.y, w[8 * c + 2], w[8 * c + 3]);
+              cvt4<FP8>(r4.z, w[8 * c + 4], w[8 * c + 5]);
+              cvt4<FP8>(r4.w, w[8 * c + 6], w[8 * c + 7]);
             }
             if (nvalid < kTileTok) {
 #pragma unroll
@@ -439,92 +704,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t lo[16], hi[16];
 #pragma unroll
             for (int k = 0; k < 16; ++k) { lo[k] = w[k]; hi[k] = w[16 + k]; }
-            tmem_st16(t_lane + TM::V + box * 32, lo);
-            tmem_st16(t_lane + TM::V + box * 32 + 16, hi);
+            tmem_st16(dst + box * 32, lo);
+            tmem_st16(dst + box * 32 + 16, hi);
           }
           tmem_wait_st();
         }
+        warp_arrive(&empty[stage], lane);
+        if (d == 0) trace_ev(p, g, 6);
+        // The first PV of item li overwrites O buffer li&1, which held item
+        // li-2, whose epilogue ran at the first tile of item li-1.
         tc_fence_before();
-        bar_sync(1, kMathThreads);
-        if (*abort_flag) { fail = true; break; }
-        if (tid == 0) {
-          mbar_arrive(&empty[stage_prev]);
-          tc_fence_after();
-          const uint32_t pbuf = p_s + (tl & 1) * NR * 256;
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd = sdesc_k128(pbuf + (kk >> 2) * NR * 128 + (kk & 3) * 32);
-            const uint32_t acc = (!first_pv || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + TM::O, tmem + TM::V + 8 * kk, bd, idesc, acc);
-            mma_ts(tmem + TM::L, tmem + TM::ONES + 8 * kk, bd, idesc, acc);
-          }
-          tc_commit(bar_pv);
-        }
-        ++pv_issued;
-        first_pv = false;
+        warp_arrive(&vready[g & 1], lane);
+        if (d == 0) trace_ev(p, g, 7);
+        // the epilogue of item li-1 runs once this tile's V is handed over
+        if (i == 0 && li > 0 && !epilogue(li - 1, g_last_prev)) break;
       }
       if (fail) break;
-
-      // ---------------- epilogue
-      if (!wait_pv_upto(pv_issued)) { note_fail(it); break; }
-      tc_fence_after();
-      float o[NR], l[NR];
-#pragma unroll
-      for (int c = 0; c < NR / 16; ++c) {
-        uint32_t v[16], u[16];
-        tmem_ld16(t_lane + TM::O + 16 * c, v);
-        tmem_ld16(t_lane + TM::L + 16 * c, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          o[16 * c + j] = __uint_as_float(v[j]);
-          l[16 * c + j] = __uint_as_float(u[j]);
-        }
-      }
-      const int d = tid;
-      const float vs = load_scale(p.v_scale, p.scale_kind,
-                                  p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * kHeadDim + d : kvh);
-      const float ln2 = 0.69314718055994530942f;
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r < n_rows) {
-          const int token = tok0 + r / G;
-          const int head = kvh * G + r % G;
-          const float inv = l[r] > 0.f ? 1.0f / l[r] : 0.f;
-          const __nv_bfloat16 val = __float2bfloat16_rn(o[r] * inv * vs);
-          if (nch == 1) {
-            p.out[((int64_t)token * p.q_heads + head) * kHeadDim + d] = val;
-            if (tid == r && p.lse != nullptr)
-              p.lse[(int64_t)token * p.q_heads + head] =
-                  l[r] > 0.f ? (m[r] + __log2f(l[r])) * ln2 : -INFINITY;
-          } else {
-            const int64_t slot = ((int64_t)token * p.max_chunks + chunk) * p.q_heads + head;
-            p.part_o[slot * kHeadDim + d] = val;
-            if (tid == r) {
-              p.part_m[slot] = l[r] > 0.f ? m[r] * ln2 : -INFINITY;
-              p.part_d[slot] = l[r];
-            }
-          }
-        }
-      }
+      g_last_prev = g - 1;
     }
-    // make sure no tensor-core op is still in flight before TMEM is released
-    if (fail) {
-      while (s_waited < s_issued) {
-        if (!mbar_wait(bar_s, s_waited & 1, limit)) break;
-        ++s_waited;
-      }
-      while (pv_waited < pv_issued) {
-        if (!mbar_wait(bar_pv, pv_waited & 1, limit)) break;
-        ++pv_waited;
-      }
-    }
+    if (!fail && item_end > item_begin) epilogue(item_end - item_begin - 1, g_last_prev);
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, TM::kCols);
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int NR, int FP8>

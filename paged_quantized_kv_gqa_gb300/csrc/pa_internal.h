@@ -36,7 +36,8 @@ struct Plan {
   std::vector<int32_t> work_indptr;  // [num_ctas+1]
   std::vector<int32_t> nch_token;    // [T]
   std::vector<int32_t> merge_tokens; // [n_merge]
-  // device blob = work_indptr | items | nch_token | merge_tokens (int32), at kStatusBytes
+  // device blob = work_indptr | items | nch_token | merge_tokens (int32), at kStatusBytes;
+  // each array starts at a multiple of 4 words (16 bytes)
   std::vector<int32_t> blob;
   size_t off_indptr = 0, off_items = 0, off_nch = 0, off_merge = 0;  // int32 offsets in blob
   size_t plan_bytes = 0;
@@ -61,6 +62,9 @@ struct WsView {
 struct FaultCfg {
   int64_t wait_limit_ns;
   int32_t skip_first_load;
+  uint64_t* trace;        // device timeline buffer or null
+  int32_t trace_ctas;
+  int32_t trace_tiles;
 };
 
 // Kernel parameter block for the attention kernels (passed by value).
@@ -88,6 +92,9 @@ struct AttnParams {
   int32_t max_chunks;
   int32_t skip_first_load;
   float sm_scale_log2;   // sm_scale * log2(e)
+  uint64_t* trace;       // [trace_ctas][trace_tiles][16] %globaltimer stamps, or null
+  int32_t trace_ctas;
+  int32_t trace_tiles;
 };
 
 void set_error(const std::string& msg);
