@@ -12,8 +12,8 @@ sequence split sized from the SM count).
 Spec:
   G = q_heads / kv_heads.  family = "mla" for the MLA layout; otherwise
   "decode" when max(q_len) * G <= 64, else "append".
-  rows_cap = 64 (decode), 128 (append), q_heads (mla); tokens per tile
-  tpt = rows_cap // G.  CTAs per item: 2 for mla, else 1; slots = num_sms //
+  rows_cap = 64 (decode), 256 (append: two 128-row query tiles), q_heads
+  (mla); tokens per tile tpt = rows_cap // G.  CTAs per item: 2 for mla, else 1; slots = num_sms //
   (CTAs per item).
   Tiles, sequence-major: for b, for t in 0..ceil(q_len_b / tpt)-1:
       tok0 = t*tpt, tok1 = min(q_len_b, tok0 + tpt),
@@ -44,7 +44,7 @@ import math
 import numpy as np
 
 DECODE_ROWS = 64
-APPEND_ROWS = 128
+APPEND_ROWS = 256
 
 
 def plan(p, num_sms: int) -> dict:

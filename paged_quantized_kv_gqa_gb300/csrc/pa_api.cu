@@ -7,7 +7,7 @@
 // item; XQA mla_sm120.cu: the SM-count-driven sub-sequence split):
 //   family: MLA layout -> MLA; else decode when max(q_len) * G <= 64, else append.
 //   tiles of tokens_per_tile = rows_cap / G query tokens (rows_cap 64 decode,
-//   128 append, q_heads MLA); lim = seq_lens_kv + tok1 (causal) or kvtot.
+//   256 append = two 128-row query tiles, q_heads MLA); lim = seq_lens_kv + tok1 (causal) or kvtot.
 //   chunk: >0 as given, 0 none, -1 auto = max(4B, roundup(ceil(W/(4*slots)), B)),
 //   W = kv_heads * sum(lim), no split if that reaches the longest lim.
 //   items (tile, kv head, chunk) in that nesting order; cost = ceil(len/B) + 2;

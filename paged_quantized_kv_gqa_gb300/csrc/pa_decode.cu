@@ -15,17 +15,18 @@
 //   * Warp specialisation, one persistent CTA of four warpgroups per SM:
 //       SM0, SM1  online softmax, each on half of the packed rows (lane =
 //                 position): running max (lazy, vote per half), row sums in
-//                 registers, P^T to shared memory, and the rare rescale of
-//                 its columns of O;
+//                 registers, P^T to shared memory, the rare rescale of its
+//                 columns of O, and the epilogue of its rows (one tile after
+//                 the item's last PV was queued);
 //       CV        Q' of each item, K rows (lane = position) and V^T rows (lane
-//                 = head dim) dequantised straight into TMEM, and the epilogue;
+//                 = head dim) dequantised straight into TMEM;
 //       IO        one TMA warp ((page, kv head) K slab [64 x 128] with 128B
 //                 swizzle and V slab [128 x 64] with 64B swizzle per page) and
 //                 one MMA warp issuing S = K Q'^T and O += V^T P^T, polling
 //                 both queues and issuing whichever is ready.
 //     The roles meet only at mbarriers: K, V and S are double-buffered, P^T
 //     four-deep, Q' and O double-buffered per item (the epilogue of an item
-//     overlaps the next item), so dequantisation, softmax, tensor-core work
+//     runs during the next item), so dequantisation, softmax, tensor-core work
 //     and page loads of neighbouring tiles and items overlap.
 //   * tcgen05.mma with M = 128 costs about the same for any N <= 64, so the
 //     kernel issues the minimum: 8 MMAs for S and 8 for PV per 128-position
@@ -55,7 +56,6 @@ constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBufs = 4;                        // P^T ring depth
-constexpr int kItemRing = 8;                     // per-item row-sum / max hand-off ring
 
 constexpr int stages_for(int nr) { return nr <= 48 ? 4 : 3; }
 
@@ -73,13 +73,12 @@ struct Smem {
   static constexpr int kP = kQ + 2 * NR * 256;             // P^T ring
   static constexpr int kRed = kP + kPBufs * NR * 256;      // [4][NR] warp maxima
   static constexpr int kRedL = kRed + 4 * NR * 4;          // [4][NR] warp row sums
-  static constexpr int kLsum = kRedL + 4 * NR * 4;         // [ring][NR] item row sums
-  static constexpr int kMfin = kLsum + kItemRing * NR * 4; // [ring][NR] item running max
-  static constexpr int kM = kMfin + kItemRing * NR * 4;    // [NR] running max
+  static constexpr int kLsum = kRedL + 4 * NR * 4;         // [2][NR] 1/l per item (by parity)
+  static constexpr int kM = kLsum + 2 * NR * 4;            // [NR] running max
   static constexpr int kAlpha = kM + NR * 4;               // [NR] rescale factors
   static constexpr int kBars = kAlpha + NR * 4;
-  // full[S], empty[S], kready[2], sfull[2], sfree[2], pready[4], vready[2], pvdone[4], lready[8]
-  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + kPBufs + 2 + kPBufs + kItemRing;
+  // full[S], empty[S], kready[2], sfull[2], sfree[2], pready[4], vready[2], pvdone[4]
+  static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + kPBufs + 2 + kPBufs;
   static constexpr int kMisc = kBars + kNumBars * 8;       // tmem addr, abort flags
   static constexpr int kTotal = kMisc + 32 + 1024;         // + alignment slack
   static_assert(kTotal <= 232448, "shared memory overflow");
@@ -179,14 +178,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pready = sfree + 2;
   uint64_t* vready = pready + kPBufs;
   uint64_t* pvdone = vready + 2;
-  uint64_t* lready = pvdone + kPBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
   volatile int* abort_any = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
   volatile int* abort_grp = reinterpret_cast<volatile int*>(smem + SM::kMisc + 8);  // [2]
   float* red = reinterpret_cast<float*>(smem + SM::kRed);
   float* red_l = reinterpret_cast<float*>(smem + SM::kRedL);
   float* lsum_s = reinterpret_cast<float*>(smem + SM::kLsum);
-  float* mfin_s = reinterpret_cast<float*>(smem + SM::kMfin);
   float* m_s = reinterpret_cast<float*>(smem + SM::kM);
   float* alpha_s = reinterpret_cast<float*>(smem + SM::kAlpha);
   const uint32_t s_base = smem_u32(smem);
@@ -217,7 +214,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&pready[j], 8);
       mbar_init(&pvdone[j], 1);
     }
-    for (int j = 0; j < kItemRing; ++j) mbar_init(&lready[j], 8);
     *abort_any = 0;
     abort_grp[0] = 0;
     abort_grp[1] = 0;
@@ -295,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint64_t t_idle = 0;
       while (cp.valid()) {
         bool progressed = false;
-        if (cs.valid() && mbar_try_wait(&kready[gs & 1], (gs >> 1) & 1) &&
-            (gs < 2 || mbar_try_wait(&sfree[gs & 1], ((gs - 2) >> 1) & 1))) {
+        if (cs.valid() && mbar_test_wait(&kready[gs & 1], (gs >> 1) & 1) &&
+            (gs < 2 || mbar_test_wait(&sfree[gs & 1], ((gs - 2) >> 1) & 1))) {
           tc_fence_after();
           const uint32_t kb = TM::K0 + (gs & 1) * 64;
           const uint32_t sd = TM::S0 + (gs & 1) * NR;
@@ -312,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           cs.advance();
           progressed = true;
         }
-        if (gp < gs && mbar_try_wait(&pready[gp & 3], (gp >> 2) & 1) &&
-            mbar_try_wait(&vready[gp & 1], (gp >> 1) & 1)) {
+        if (gp < gs && mbar_test_wait(&pready[gp & 3], (gp >> 2) & 1) &&
+            mbar_test_wait(&vready[gp & 1], (gp >> 1) & 1)) {
           tc_fence_after();
           const uint32_t vb = TM::V0 + (gp & 1) * 64;
           const uint32_t pb = p_s + (gp & 3) * NR * 256;
@@ -365,6 +361,52 @@ __global__ void __launch_bounds__(kThreads, 1)
       *my_abort = 1;
       fail = true;
     };
+    // epilogue of local item li (last tile gl) for this warpgroup's rows:
+    // O^T row d = this thread's TMEM lane, times 1/l and the V scale
+    auto epilogue = [&](int li, uint32_t gl) -> bool {
+      const int it = item_begin + li;
+      const Item m = load_item(p.items, it);
+      if (!wait_or_abort(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
+        note_fail(it);
+        return false;
+      }
+      tc_fence_after();
+      const int d = pos_in_tile;
+      uint32_t v[NH];
+#pragma unroll
+      for (int c = 0; c < NH / 8; ++c)
+        tmem_ld8(t_lane + TM::O0 + (li & 1) * NR + r_lo + 8 * c,
+                 *reinterpret_cast<uint32_t(*)[8]>(&v[8 * c]));
+      tmem_wait_ld();
+      tc_fence_before();
+      const float vs = load_scale(p.v_scale, p.scale_kind,
+                                  p.scale_kind == PA_SCALE_PER_CHANNEL ? m.kvh * kHeadDim + d : m.kvh);
+      const float* inv = lsum_s + (li & 1) * NR;
+      const int n_rows = m.ntok * G;
+      int token = m.tok0 + r_lo / G, gq = r_lo % G;   // row r_lo + j <-> (token, gq)
+#pragma unroll
+      for (int j = 0; j < NH; ++j) {
+        if (r_lo + j < n_rows) {
+          const int head = m.kvh * G + gq;
+          const __nv_bfloat16 val =
+              __float2bfloat16_rn(__uint_as_float(v[j]) * inv[r_lo + j] * vs);
+          if (m.nch == 1) {
+            p.out[((int64_t)token * p.q_heads + head) * kHeadDim + d] = val;
+          } else {
+            const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
+            p.part_o[sp * kHeadDim + d] = val;
+          }
+        }
+        if (++gq == G) {
+          gq = 0;
+          ++token;
+        }
+      }
+      if (tid == 0) trace_ev(p, gl, 10);
+      return true;
+    };
+    int pend_li = -1;
+    uint32_t pend_g = 0;
     uint32_t g = 0;
     float l[NH];
     for (int it = item_begin; it < item_end && !stop; ++it) {
@@ -383,14 +425,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if (tid == 0) trace_ev(p, g, 3);
         if (!fail) {
+          uint32_t v[NH];
 #pragma unroll
-          for (int c = 0; c < NH / 8; ++c) {
-            uint32_t v[8];
-            tmem_ld8(t_lane + TM::S0 + (g & 1) * NR + r_lo + 8 * c, v);
-            tmem_wait_ld();
+          for (int c = 0; c < NH / 8; ++c)
+            tmem_ld8(t_lane + TM::S0 + (g & 1) * NR + r_lo + 8 * c,
+                     *reinterpret_cast<uint32_t(*)[8]>(&v[8 * c]));
+          tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) s[8 * c + j] = __uint_as_float(v[j]);
-          }
+          for (int j = 0; j < NH; ++j) s[j] = __uint_as_float(v[j]);
         } else {
 #pragma unroll
           for (int j = 0; j < NH; ++j) s[j] = 0.f;
@@ -502,8 +544,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         warp_arrive(&pready[g & 3], lane);
         if (tid == 0) trace_ev(p, g, 4);
+        // epilogue of the previous item, one tile after its last PV was queued
+        if (pend_li >= 0 && pend_li < li) {
+          if (!epilogue(pend_li, pend_g)) { stop = true; break; }
+          pend_li = -1;
+        }
         if (i + 1 == cur.ntiles) {
-          // row sums over all positions of the item: warp, then warpgroup
+          // row sums over all positions of the item: warp, then warpgroup; the
+          // owner thread of row r keeps 1/l and writes the row statistics
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
             float v = l[j];
@@ -512,20 +560,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) red_l[(warp & 3) * NR + r_lo + j] = v;
           }
           bar_sync(bar_id, 128);
-          const int slot = li & (kItemRing - 1);
           if (pos_in_tile < NH) {
             const int r = r_lo + pos_in_tile;
-            lsum_s[slot * NR + r] = red_l[r] + red_l[NR + r] + red_l[2 * NR + r] + red_l[3 * NR + r];
-            mfin_s[slot * NR + r] = m_s[r];
+            const float lr = red_l[r] + red_l[NR + r] + red_l[2 * NR + r] + red_l[3 * NR + r];
+            lsum_s[(li & 1) * NR + r] = lr > 0.f ? __frcp_rn(lr) : 0.f;
+            if (r < n_rows) {
+              const int token = cur.tok0 + r / G;
+              const int head = cur.kvh * G + r % G;
+              const float mr = m_s[r];
+              const float ln2 = 0.69314718055994530942f;
+              if (cur.nch == 1) {
+                if (p.lse != nullptr)
+                  p.lse[(int64_t)token * p.q_heads + head] =
+                      lr > 0.f ? (mr + __log2f(lr)) * ln2 : -INFINITY;
+              } else {
+                const int64_t sp = ((int64_t)token * p.max_chunks + cur.chunk) * p.q_heads + head;
+                p.part_m[sp] = lr > 0.f ? mr * ln2 : -INFINITY;
+                p.part_d[sp] = lr;
+              }
+            }
           }
-          warp_arrive(&lready[slot], lane);
+          bar_sync(bar_id, 128);  // 1/l of this item visible to the warpgroup
+          pend_li = li;
+          pend_g = g;
         }
       }
     }
+    if (!stop && pend_li >= 0) epilogue(pend_li, pend_g);
   } else {
     // ================================================================ CV warpgroup
     // Q' of each item, K rows (lane = position) and V^T rows (lane = head dim)
-    // into TMEM, and the epilogue of each item (deferred by one item)
+    // into TMEM
     const int d = tid & 127;  // TMEM lane: K position / V head dim / output dim
     uint32_t g = 0;
     bool fail = false;
@@ -567,65 +632,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
     };
-    // epilogue of local item li (tiles ending at global tile gl): O / row sum
-    auto epilogue = [&](int li, uint32_t gl) -> bool {
-      const int it = item_begin + li;
-      const Item m = load_item(p.items, it);
-      const int slot = li & (kItemRing - 1);
-      if (!wait_or_abort(&lready[slot], (li / kItemRing) & 1, limit, abort_any) ||
-          !wait_or_abort(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
-        note_fail(it);
-        return false;
-      }
-      tc_fence_after();
-      float o[NR];
-      const uint32_t ob = TM::O0 + (li & 1) * NR;
-#pragma unroll
-      for (int c = 0; c < NR / 16; ++c) {
-        uint32_t v[16];
-        tmem_ld16(t_lane + ob + 16 * c, v);
-        tmem_wait_ld();
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[16 * c + j] = __uint_as_float(v[j]);
-      }
-      tc_fence_before();
-      const float* mf = mfin_s + slot * NR;
-      const float* ls = lsum_s + slot * NR;
-      const int n_rows = m.ntok * G;
-      const float vs = load_scale(p.v_scale, p.scale_kind,
-                                  p.scale_kind == PA_SCALE_PER_CHANNEL ? m.kvh * kHeadDim + d : m.kvh);
-      const float ln2 = 0.69314718055994530942f;
-      int token = m.tok0, gq = 0;   // row r <-> (token, head-in-group gq)
-#pragma unroll
-      for (int r = 0; r < NR; ++r) {
-        if (r < n_rows) {
-          const int head = m.kvh * G + gq;
-          const float lr = ls[r];
-          const float inv = lr > 0.f ? 1.0f / lr : 0.f;
-          const __nv_bfloat16 val = __float2bfloat16_rn(o[r] * inv * vs);
-          if (m.nch == 1) {
-            p.out[((int64_t)token * p.q_heads + head) * kHeadDim + d] = val;
-            if (d == r && p.lse != nullptr)
-              p.lse[(int64_t)token * p.q_heads + head] =
-                  lr > 0.f ? (mf[r] + __log2f(lr)) * ln2 : -INFINITY;
-          } else {
-            const int64_t slot_p = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
-            p.part_o[slot_p * kHeadDim + d] = val;
-            if (d == r) {
-              p.part_m[slot_p] = lr > 0.f ? mf[r] * ln2 : -INFINITY;
-              p.part_d[slot_p] = lr;
-            }
-          }
-        }
-        if (++gq == G) {
-          gq = 0;
-          ++token;
-        }
-      }
-      if (d == 0) trace_ev(p, gl, 10);
-      return true;
-    };
-    uint32_t g_last_prev = 0;   // last tile of the previous item
     for (int it = item_begin; it < item_end && !fail; ++it) {
       const Item m = load_item(p.items, it);
       const int li = it - item_begin;
@@ -711,18 +717,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         warp_arrive(&empty[stage], lane);
         if (d == 0) trace_ev(p, g, 6);
-        // The first PV of item li overwrites O buffer li&1, which held item
-        // li-2, whose epilogue ran at the first tile of item li-1.
         tc_fence_before();
         warp_arrive(&vready[g & 1], lane);
         if (d == 0) trace_ev(p, g, 7);
-        // the epilogue of item li-1 runs once this tile's V is handed over
-        if (i == 0 && li > 0 && !epilogue(li - 1, g_last_prev)) break;
       }
-      if (fail) break;
-      g_last_prev = g - 1;
     }
-    if (!fail && item_end > item_begin) epilogue(item_end - item_begin - 1, g_last_prev);
   }
 
   tc_fence_before();

@@ -16,7 +16,7 @@ namespace pa {
 
 constexpr int kItemWords = 8;        // b, kvh, token0, n_tok, causal_base, kv0, kv1, c|nch<<16
 constexpr int kDecodeRows = 64;      // packed (token, head) rows per decode tile
-constexpr int kAppendRows = 128;     // packed rows per append tile
+constexpr int kAppendRows = 256;     // packed rows per append item (two 128-row tiles)
 constexpr int kStatusBytes = 256;    // status block at the start of the workspace
 constexpr int64_t kDefaultWaitNs = 2000000000LL;
 
