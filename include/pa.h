@@ -176,10 +176,13 @@ size_t pa_workspace_size(const pa_plan_t* plan);
  * workspace: device, >= pa_workspace_size bytes, 256-byte aligned. */
 pa_status pa_plan_upload(const pa_plan_t* plan, void* workspace, void* stream);
 
-/* Enqueues the attention kernels for every work item.  Items that cover the
- * whole KV range of their rows write out/lse directly; split rows write
- * partial states into the workspace and need pa_merge afterwards.  The
- * workspace must hold this plan (pa_plan_upload). */
+/* Enqueues the attention kernel of the plan's family for every work item
+ * (decode: q_len * G <= 64 packed rows per tile; append: 256 packed rows per
+ * item, out must be 16-byte aligned).  Items that cover the whole KV range of
+ * their rows write out/lse directly; split rows write partial states into the
+ * workspace and need pa_merge afterwards.  The workspace must hold this plan
+ * (pa_plan_upload).  PA_ERR_UNSUPPORTED for a family whose kernel is not
+ * compiled into this build. */
 pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, void* stream);
 
 /* Enqueues the log-sum-exp merge of the partial states of split rows into

@@ -304,6 +304,24 @@ static pa_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint6
   return PA_OK;
 }
 
+// Query rows [T][Hq][128] bf16 (token stride q_stride elements) as a 3-D map
+// with a box of {64 dims, G heads, box_tok tokens}, 128B swizzle: one box is
+// one k-half of an item's packed (token, head-in-group) rows.
+static pa_status make_map_q(CUtensorMap* m, const void* q, uint64_t tokens, uint64_t heads,
+                            int64_t q_stride, uint32_t box_heads, uint32_t box_tok) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
+  const cuuint64_t dims[3] = {128, heads, tokens};
+  const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)q_stride * 2};
+  const cuuint32_t box[3] = {64, box_heads, box_tok};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled (query map) failed");
+  return PA_OK;
+}
+
 static pa_status check_args(const Plan& P, const pa_args* a, bool need_cache) {
   if (!a) return fail(PA_ERR_INVALID_ARG, "null pa_args");
   if (!a->out) return fail(PA_ERR_INVALID_ARG, "null out");
@@ -438,6 +456,22 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
     s = make_map(&tv, args->cache_v, heads_total * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
     if (s != PA_OK) return s;
     e = launch_decode(*plan, p, tk, tv, st);
+  } else if (plan->family == PA_FAMILY_APPEND) {
+    if (reinterpret_cast<uintptr_t>(args->out) % 16)
+      return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    CUtensorMap tk, tv, tq;
+    const uint64_t heads_total = (uint64_t)pr.num_pages * pr.kv_heads;
+    s = make_map(&tk, args->cache_k, heads_total * 64, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != PA_OK) return s;
+    s = make_map(&tv, args->cache_v, heads_total * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (s != PA_OK) return s;
+    const int G = pr.q_heads / pr.kv_heads;
+    const int box_tok = std::min(plan->tokens_per_tile, plan->total_q);
+    s = make_map_q(&tq, args->q, (uint64_t)plan->total_q, (uint64_t)pr.q_heads, pr.q_stride,
+                   (uint32_t)G, (uint32_t)box_tok);
+    if (s != PA_OK) return s;
+    p.q_box_tokens = box_tok;
+    e = launch_append(*plan, p, tk, tv, tq, st);
   } else {
     return fail(PA_ERR_UNSUPPORTED, "kernel family not built yet");
   }

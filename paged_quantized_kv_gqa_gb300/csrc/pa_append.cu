@@ -1,0 +1,578 @@
+// pa_append.cu - paged int8 / FP8-E4M3 KV attention for many packed query rows
+// (chunked-prefill "append": q_len * G > 64), tcgen05 + TMA, sm_103a.
+//
+// Operation: FastDeploy append_attention_c8_impl.cuh,
+// multi_query_append_attention_c8_kernel (a CTA row per (sequence, q tile,
+// kv head) whose query rows pack (token, head-in-group); query token i of the
+// sequence sees positions j <= seq_lens_kv + i; chunk bounds
+// [c*chunk, min(lim, (c+1)*chunk)); direct write for one chunk, else partial
+// o plus tmp_m / tmp_d for the merge).  The sm80 design there (cp.async +
+// mma.sync, dequantisation inside the MMA fragments) is replaced by:
+//
+//   * Rows as M.  An item holds 256 packed rows, two 128-row query tiles A
+//     and B that share every K/V tile.  Per 128-position KV tile and query
+//     tile: S = Q' K^T is one 128x128 fp32 accumulator in TMEM (8 x
+//     tcgen05.mma, K = 16 each); P (fp16) overwrites S in TMEM and is the TMEM
+//     A operand of O += P V (8 more MMAs), O being 128x128 fp32 in TMEM.
+//     TMEM: S_A 0, S_B 128, O_A 256, O_B 384 (all 512 columns).
+//   * One persistent CTA of four warpgroups per SM:
+//       SM_A, SM_B  softmax of query tile A / B, thread = row: exact row max
+//                   of the tile, lazy rescale (threshold 2^8) of l and of the
+//                   thread's O row in TMEM, P into TMEM, epilogue of its row;
+//       CV          Q' (bf16 -> fp16 times the per-channel K scale, in place)
+//                   and the K / V tiles, int8 or e4m3 -> fp16 (exact), into
+//                   128B-swizzled K-major shared memory: K as the B operand of
+//                   S (rows = positions), V^T as the B operand of PV (rows =
+//                   head dims, which is the cache's own V layout);
+//       IO          one TMA warp (the item's Q rows as a 3-D box, K and V page
+//                   slabs into a 3-stage ring) and two MMA-issue warps, one
+//                   per query tile, so each tile's S -> softmax -> PV chain
+//                   runs independently and the tensor pipe interleaves them.
+//   * Ordering rules that make the single-buffered S/P, K16, V16 and Q' safe:
+//     S_X(t) is issued only after PV_X(t-1) completed (P_X is read by it, and
+//     O_X is then quiescent for the softmax's rescale), K16 / V16 / Q' are
+//     rewritten only after both chains' MMAs that read them completed
+//     (tcgen05.commit to two-arrival barriers).
+//   * Per-kv-head / global K scales fold into the softmax scale, V scales into
+//     the epilogue, per-channel K scales into Q'.
+#include <cfloat>
+
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kTile = 128;                       // KV positions per tile
+constexpr int kHeadDim = 128;
+constexpr int kPage = 64;
+constexpr int kRows = 256;                       // packed query rows per item
+constexpr int kSlab = kPage * kHeadDim;          // bytes of one (page, head) K or V slab
+constexpr int kStageBytes = 4 * kSlab;           // K (2 pages) + V (2 pages)
+constexpr int kStages = 3;
+constexpr float kTau = 8.0f;                     // lazy-rescale threshold (log2 units)
+constexpr int kThreads = 512;
+constexpr int kWarpTma = 12;
+constexpr int kWarpMma0 = 13;                    // issues the MMAs of query tile A
+constexpr int kWarpMma1 = 14;                    // ... of query tile B
+constexpr uint32_t kTmemCols = 512;
+constexpr int kCvBar = 3;                        // named barrier of the CV warpgroup
+
+struct Smem {
+  static constexpr int kRaw = 0;                              // [kStages][K0 K1 V0 V1]
+  static constexpr int kQ = kStages * kStageBytes;            // [2 k-halves][256 rows][128 B]
+  static constexpr int kK16 = kQ + kRows * 256;               // [2][128 positions][128 B]
+  static constexpr int kV16 = kK16 + kTile * 256;             // [2][128 dims][128 B]
+  static constexpr int kKsc = kV16 + kTile * 256;             // [128] fp32 per-channel K scale
+  static constexpr int kBars = kKsc + kHeadDim * 4;
+  // full[S] empty[S] qfull qready qfree kready kfree vready vfree sfull[2] pready[2] pvdone[2]
+  static constexpr int kNumBars = 2 * kStages + 7 + 6;
+  static constexpr int kMisc = kBars + kNumBars * 8;          // tmem address, abort flag
+  static constexpr int kTotal = kMisc + 16 + 1024;            // + alignment slack
+  static_assert(kTotal <= 232448, "shared memory overflow");
+};
+
+// Shared-memory descriptor of k-step kk (16 elements) of a K-major SW128
+// operand whose two 64-element halves are `half_bytes` apart.
+__device__ __forceinline__ uint64_t kstep_desc(uint32_t base, int kk, int half_bytes) {
+  return sdesc_k128(base + (kk >> 2) * half_bytes + (kk & 3) * 32);
+}
+
+}  // namespace
+
+template <int FP8>
+__global__ void __launch_bounds__(kThreads, 1)
+    append_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  using SM = Smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBars);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kStages;
+  uint64_t* qfull = empty + kStages;
+  uint64_t* qready = qfull + 1;
+  uint64_t* qfree = qready + 1;
+  uint64_t* kready = qfree + 1;
+  uint64_t* kfree = kready + 1;
+  uint64_t* vready = kfree + 1;
+  uint64_t* vfree = vready + 1;
+  uint64_t* sfull = vfree + 1;     // [2]
+  uint64_t* pready = sfull + 2;    // [2]
+  uint64_t* pvdone = pready + 2;   // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
+  volatile int* abort_any = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t q_s = s_base + SM::kQ;
+  const uint32_t k16 = s_base + SM::kK16;
+  const uint32_t v16 = s_base + SM::kV16;
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int wg = warp >> 2;         // warpgroup: 0, 1 softmax A / B; 2 CV; 3 IO
+  const int item_begin = p.work_indptr[blockIdx.x];
+  const int item_end = p.work_indptr[blockIdx.x + 1];
+  const uint64_t limit = (uint64_t)p.wait_limit_ns;
+  const int G = p.group;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    mbar_init(qfull, 1);
+    mbar_init(qready, 4);
+    mbar_init(qfree, 2);
+    mbar_init(kready, 4);
+    mbar_init(kfree, 2);
+    mbar_init(vready, 4);
+    mbar_init(vfree, 2);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&sfull[x], 1);
+      mbar_init(&pready[x], 4);
+      mbar_init(&pvdone[x], 1);
+    }
+    *abort_any = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // this warp's TMEM lane quarter (a warp may only touch lanes 32*(warp%4) ..)
+  const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+
+  if (warp == kWarpTma) {
+    // ================================================================ TMA
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_q);
+      const int box_tok = p.q_box_tokens;
+      const uint32_t qbytes = 2u * 128u * (uint32_t)(G * box_tok);
+      uint32_t g = 0;
+      int issued_g[kStages];
+      for (int s = 0; s < kStages; ++s) issued_g[s] = -1;
+      int q_issued = 0;
+      bool ok = true;
+      for (int it = item_begin; it < item_end && ok; ++it) {
+        const Item m = load_item<kTile>(p.items, it);
+        const int li = it - item_begin;
+        const int32_t* bt = p.block_table + (int64_t)m.b * p.max_blocks;
+        // Q rows of the item (both k-halves); the buffer is free once both
+        // chains' S MMAs of the previous item completed
+        if (li > 0 && !wait_or_abort(qfree, (li - 1) & 1, limit, abort_any)) {
+          if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+          *abort_any = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(qfull, qbytes);
+        tma_load_3d(smem + SM::kQ, &tm_q, qfull, 0, m.kvh * G, m.tok0);
+        tma_load_3d(smem + SM::kQ + kRows * 128, &tm_q, qfull, 64, m.kvh * G, m.tok0);
+        ++q_issued;
+        for (int t = 0; t < m.ntiles; ++t, ++g) {
+          const int stage = g % kStages;
+          const uint32_t ph = (g / kStages) & 1;
+          const int pos0 = m.kv0 + t * kTile;
+          const int npg = (m.kv1 - pos0) > kPage ? 2 : 1;
+          int pages[2];
+          pages[0] = bt[pos0 / kPage];
+          pages[1] = npg == 2 ? bt[pos0 / kPage + 1] : 0;
+          if (!wait_or_abort(&empty[stage], ph ^ 1, limit, abort_any)) {
+            if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+            *abort_any = 1;
+            ok = false;
+            break;
+          }
+          if (p.skip_first_load && g == 0) continue;  // failure-detection test hook
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(npg * 2 * kSlab));
+          issued_g[stage] = (int)g;
+          uint8_t* st = smem + SM::kRaw + stage * kStageBytes;
+          for (int pg = 0; pg < npg; ++pg) {
+            const int page = pages[pg];
+            int yk, yv;
+            if (page < 0 || page >= p.num_pages) {
+              record_status(p.status, PA_ERR_BAD_PAGE, it);
+              yk = p.num_pages * p.kv_heads * kPage;       // past the end: TMA fills zeros
+              yv = p.num_pages * p.kv_heads * kHeadDim;
+            } else {
+              yk = (page * p.kv_heads + m.kvh) * kPage;
+              yv = (page * p.kv_heads + m.kvh) * kHeadDim;
+            }
+            tma_load_2d(st + pg * kSlab, &tm_k, &full[stage], 0, yk);
+            tma_load_2d(st + 2 * kSlab + pg * kSlab, &tm_v, &full[stage], 0, yv);
+          }
+        }
+      }
+      // every issued load lands before the CTA exits
+      for (int s = 0; s < kStages; ++s)
+        if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, limit);
+      if (q_issued > 0) mbar_wait(qfull, (q_issued - 1) & 1, limit);
+    }
+  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
+    // ================================================================ MMA issue
+    // chain X: S_X(t) = Q'_X K16^T, then O_X += P_X V16, tile after tile
+    if (lane == 0) {
+      const int X = warp - kWarpMma0;
+      const uint32_t idesc = idesc_f16_f32(128, 128);
+      const uint32_t s_tm = tmem + X * 128;
+      const uint32_t o_tm = tmem + 256 + X * 128;
+      const uint32_t qa = q_s + X * 128 * 128;
+      uint32_t g = 0, gx = 0, n_s = 0;
+      bool ok = true;
+      for (int it = item_begin; it < item_end && ok; ++it) {
+        const Item m = load_item<kTile>(p.items, it);
+        const int li = it - item_begin;
+        const bool active = X == 0 || m.ntok * G > 128;
+        if (!wait_or_abort(qready, li & 1, limit, abort_any)) { ok = false; break; }
+        for (int i = 0; i < m.ntiles; ++i, ++g) {
+          if (!wait_or_abort(kready, g & 1, limit, abort_any)) { ok = false; break; }
+          if (active) {
+            if (gx > 0 && !wait_or_abort(&pvdone[X], (gx - 1) & 1, limit, abort_any)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(s_tm, kstep_desc(qa, kk, kRows * 128), kstep_desc(k16, kk, kTile * 128), idesc,
+                     kk > 0 ? 1u : 0u);
+            tc_commit(&sfull[X]);
+            ++n_s;
+          }
+          tc_commit(kfree);
+          if (i + 1 == m.ntiles) tc_commit(qfree);
+          if (!wait_or_abort(vready, g & 1, limit, abort_any)) { ok = false; break; }
+          if (active) {
+            if (!wait_or_abort(&pready[X], gx & 1, limit, abort_any)) { ok = false; break; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(o_tm, s_tm + 8 * kk, kstep_desc(v16, kk, kTile * 128), idesc,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&pvdone[X]);
+            ++gx;
+          }
+          tc_commit(vfree);
+        }
+      }
+      if (!ok) {
+        if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
+        *abort_any = 1;
+      }
+      // drain: every MMA this thread issued completes before TMEM is released
+      if (n_s > 0) mbar_wait(&sfull[X], (n_s - 1) & 1, limit);
+      if (gx > 0) mbar_wait(&pvdone[X], (gx - 1) & 1, limit);
+    }
+  } else if (wg == 3) {
+    // warp 15: no role (it completes the fourth warpgroup)
+  } else if (wg < 2) {
+    // ================================================================ softmax
+    // query tile X; this thread owns packed row r = 128 X + (TMEM lane)
+    const int X = wg;
+    const int rr = tid & 127;
+    const int r = X * 128 + rr;
+    const uint32_t s_tm = t_lane + X * 128;
+    const uint32_t o_tm = t_lane + 256 + X * 128;
+    uint32_t gx = 0;
+    bool fail = false;
+    for (int it = item_begin; it < item_end && !fail; ++it) {
+      const Item m = load_item<kTile>(p.items, it);
+      if (!(X == 0 || m.ntok * G > 128)) continue;   // tile B holds no rows of this item
+      const int n_rows = m.ntok * G;
+      const bool row_ok = r < n_rows;
+      const int tok = r / G;
+      const float c_log2 = p.sm_scale_log2 *
+          (p.scale_kind == PA_SCALE_PER_CHANNEL ? 1.0f : load_scale(p.k_scale, p.scale_kind, m.kvh));
+      // positions < vis_lim are visible to this row (prefix rule; cbase is the
+      // causal base, or kvtot without a causal mask)
+      const int vis_lim = min(m.kv1, m.cbase + tok + 1);
+      float m_run = -INFINITY, l = 0.0f;
+      for (int i = 0; i < m.ntiles; ++i, ++gx) {
+        if (!wait_or_abort(&sfull[X], gx & 1, limit, abort_any)) {
+          if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+          *abort_any = 1;
+          fail = true;
+          break;
+        }
+        tc_fence_after();
+        const int nvis = max(0, min(kTile, vis_lim - (m.kv0 + i * kTile)));
+        // ---- pass 1: maximum of the visible raw scores
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t v[32];
+          tmem_ld16(s_tm + 32 * q4, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tmem_ld16(s_tm + 32 * q4 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+          tmem_wait_ld();
+          if (nvis >= 32 * q4 + 32) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (32 * q4 + e < nvis) mx = fmaxf(mx, __uint_as_float(v[e]));
+          }
+        }
+        const float m_tile = mx * c_log2;   // log2 units; -inf when nothing is visible
+        const bool need = m_tile > m_run + kTau;
+        float alpha = 1.0f;
+        if (need) {
+          alpha = (m_run == -INFINITY) ? 0.0f : fast_exp2(m_run - m_tile);
+          l *= alpha;
+          m_run = m_tile;
+        }
+        // O_X holds the PV of earlier tiles of this item: rescale this row.
+        // PV_X of the previous tile completed before S_X of this one was issued.
+        if (i > 0 && __any_sync(0xffffffffu, need)) {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t v[16];
+            tmem_ld16(o_tm + 16 * c, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tmem_st16(o_tm + 16 * c, v);
+          }
+          tmem_wait_st();
+        }
+        // ---- pass 2: P = 2^(s c - m) over the visible positions, written as
+        // fp16 over the S columns already consumed
+        const float neg_m = m_run == -INFINITY ? 0.0f : -m_run;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t v[32];
+          tmem_ld16(s_tm + 32 * q4, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+          tmem_ld16(s_tm + 32 * q4 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
+          tmem_wait_ld();
+          uint32_t w[16];
+          if (nvis >= 32 * q4 + 32) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), c_log2, neg_m));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c_log2, neg_m));
+              l += p0 + p1;
+              w[e] = pack_half2(p0, p1);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int j = 32 * q4 + 2 * e;
+              const float p0 =
+                  j < nvis ? fast_exp2(fmaf(__uint_as_float(v[2 * e]), c_log2, neg_m)) : 0.0f;
+              const float p1 =
+                  j + 1 < nvis ? fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c_log2, neg_m))
+                               : 0.0f;
+              l += p0 + p1;
+              w[e] = pack_half2(p0, p1);
+            }
+          }
+          tmem_st16(s_tm + 16 * q4, w);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(&pready[X], lane);
+      }
+      if (fail) break;
+      // ---- epilogue: O row / l times the V scale
+      if (!wait_or_abort(&pvdone[X], (gx - 1) & 1, limit, abort_any)) {
+        if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+        *abort_any = 1;
+        fail = true;
+        break;
+      }
+      tc_fence_after();
+      const float inv_l = l > 0.0f ? __frcp_rn(l) : 0.0f;
+      const bool pc = p.scale_kind == PA_SCALE_PER_CHANNEL;
+      const float vs = pc ? 1.0f : load_scale(p.v_scale, p.scale_kind, m.kvh);
+      const int token = m.tok0 + tok;
+      const int head = m.kvh * G + (r - tok * G);
+      __nv_bfloat16* dst;
+      if (m.nch == 1) {
+        dst = p.out + ((int64_t)token * p.q_heads + head) * kHeadDim;
+      } else {
+        const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
+        dst = p.part_o + sp * kHeadDim;
+      }
+      const __nv_bfloat16* vsc =
+          reinterpret_cast<const __nv_bfloat16*>(p.v_scale) + m.kvh * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t v[16];
+        tmem_ld16(o_tm + 16 * c, v);
+        tmem_wait_ld();
+        if (row_ok) {
+          uint32_t w[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float a0 = __uint_as_float(v[2 * e]) * inv_l;
+            float a1 = __uint_as_float(v[2 * e + 1]) * inv_l;
+            if (pc) {
+              a0 *= __bfloat162float(vsc[16 * c + 2 * e]);
+              a1 *= __bfloat162float(vsc[16 * c + 2 * e + 1]);
+            } else {
+              a0 *= vs;
+              a1 *= vs;
+            }
+            __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
+            w[e] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
+          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+      if (row_ok) {
+        const float ln2 = 0.69314718055994530942f;
+        if (m.nch == 1) {
+          if (p.lse != nullptr)
+            p.lse[(int64_t)token * p.q_heads + head] =
+                l > 0.0f ? (m_run + __log2f(l)) * ln2 : -INFINITY;
+        } else {
+          const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
+          p.part_m[sp] = l > 0.0f ? m_run * ln2 : -INFINITY;
+          p.part_d[sp] = l;
+        }
+      }
+      tc_fence_before();
+    }
+  } else {
+    // ================================================================ CV warpgroup
+    const int t = tid & 127;          // K position / V head dim of the tile
+    float* ksc = reinterpret_cast<float*>(smem + SM::kKsc);
+    uint32_t g = 0;
+    bool fail = false;
+    auto note_fail = [&](int it) {
+      if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+      *abort_any = 1;
+      fail = true;
+    };
+    for (int it = item_begin; it < item_end && !fail; ++it) {
+      const Item m = load_item<kTile>(p.items, it);
+      const int li = it - item_begin;
+      const bool pc = p.scale_kind == PA_SCALE_PER_CHANNEL;
+      const float sc_t = pc ? load_scale(p.k_scale, PA_SCALE_PER_CHANNEL, m.kvh * kHeadDim + t) : 1.0f;
+      if (!wait_or_abort(qfull, li & 1, limit, abort_any)) { note_fail(it); break; }
+      // Q' = bf16 Q (times the per-channel K scale) -> fp16, in place
+      bar_sync(kCvBar, 128);   // the previous item's conversion is done with ksc
+      ksc[t] = sc_t;
+      bar_sync(kCvBar, 128);
+      for (int task = t; task < kRows * 16; task += 128) {
+        const int row = task >> 4, ch = task & 15;
+        const int kb = ch >> 3, cc = ch & 7;
+        const uint32_t addr = q_s + kb * kRows * 128 + row * 128 + ((cc ^ (row & 7)) << 4);
+        const uint4 raw = ld_shared_v4(addr);
+        const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+        float f[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          f[e] = __bfloat162float(hv[e]);
+          if (pc) f[e] *= ksc[ch * 8 + e];
+        }
+        uint4 packed;
+        packed.x = pack_half2(f[0], f[1]);
+        packed.y = pack_half2(f[2], f[3]);
+        packed.z = pack_half2(f[4], f[5]);
+        packed.w = pack_half2(f[6], f[7]);
+        st_shared_v4(addr, packed);
+      }
+      fence_proxy_async_smem();
+      warp_arrive(qready, lane);
+      for (int i = 0; i < m.ntiles; ++i, ++g) {
+        const int stage = g % kStages;
+        const uint32_t st = s_base + SM::kRaw + stage * kStageBytes;
+        if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
+        const int nvalid = min(kTile, m.kv1 - (m.kv0 + i * kTile));
+        // ---- K row of position t -> K16 (rows = positions, two 64-dim halves)
+        if (g > 0 && !wait_or_abort(kfree, (g - 1) & 1, limit, abort_any)) { note_fail(it); break; }
+        {
+          const int pg = t >> 6, row = t & 63;
+          const uint32_t src = st + pg * kSlab + row * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (t < nvalid) {
+              const uint4 r4 = ld_shared_v4(src + ((c ^ (row & 7)) << 4));
+              cvt4<FP8>(r4.x, o0.x, o0.y);
+              cvt4<FP8>(r4.y, o0.z, o0.w);
+              cvt4<FP8>(r4.z, o1.x, o1.y);
+              cvt4<FP8>(r4.w, o1.z, o1.w);
+            }
+            // raw chunk c = dims 16c..16c+15 = fp16 chunks 2c, 2c+1 of half c/4
+            const uint32_t dst = k16 + (c >> 2) * kTile * 128 + t * 128;
+            const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
+            st_shared_v4(dst + ((c0 ^ (t & 7)) << 4), o0);
+            st_shared_v4(dst + ((c1 ^ (t & 7)) << 4), o1);
+          }
+        }
+        fence_proxy_async_smem();
+        warp_arrive(kready, lane);
+        // ---- V^T row of head dim t -> V16 (rows = dims, one half per page);
+        // positions past kv1 are zero so that P = 0 there meets finite values
+        if (g > 0 && !wait_or_abort(vfree, (g - 1) & 1, limit, abort_any)) { note_fail(it); break; }
+        {
+#pragma unroll
+          for (int pg = 0; pg < 2; ++pg) {
+            const uint32_t src = st + 2 * kSlab + pg * kSlab + t * 64;
+            const uint32_t dst = v16 + pg * kTile * 128 + t * 128;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int pos = pg * 64 + 16 * c;   // first tile position of this raw chunk
+              uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+              if (pos < nvalid) {
+                const uint4 r4 = ld_shared_v4(src + ((c ^ ((t >> 1) & 3)) << 4));
+                cvt4<FP8>(r4.x, o0.x, o0.y);
+                cvt4<FP8>(r4.y, o0.z, o0.w);
+                cvt4<FP8>(r4.z, o1.x, o1.y);
+                cvt4<FP8>(r4.w, o1.z, o1.w);
+                if (pos + 16 > nvalid) {
+                  uint32_t ww[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) {
+                    const int q = pos + 2 * k;
+                    if (q >= nvalid) ww[k] = 0u;
+                    else if (q + 1 >= nvalid) ww[k] &= 0x0000FFFFu;
+                  }
+                  o0 = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+                  o1 = make_uint4(ww[4], ww[5], ww[6], ww[7]);
+                }
+              }
+              const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
+              st_shared_v4(dst + ((c0 ^ (t & 7)) << 4), o0);
+              st_shared_v4(dst + ((c1 ^ (t & 7)) << 4), o1);
+            }
+          }
+        }
+        fence_proxy_async_smem();
+        warp_arrive(vready, lane);
+        warp_arrive(&empty[stage], lane);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+template <int FP8>
+static cudaError_t launch_t(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
+                            const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream) {
+  auto kern = append_kernel<FP8>;
+  const int smem = Smem::kTotal;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<plan.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, tm_q, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream) {
+  return plan.prob.kv_dtype == PA_KV_FP8_E4M3 ? launch_t<1>(plan, p, tm_k, tm_v, tm_q, stream)
+                                              : launch_t<0>(plan, p, tm_k, tm_v, tm_q, stream);
+}
+
+}  // namespace pa

@@ -38,9 +38,8 @@
 //     the epilogue, per-channel K scales into Q'.
 #include <cfloat>
 
-#include "pa_internal.h"
+#include "pa_common.cuh"
 #include "pa_index.cuh"
-#include "pa_ptx.cuh"
 
 namespace pa {
 namespace {
@@ -84,57 +83,6 @@ struct Smem {
   static_assert(kTotal <= 232448, "shared memory overflow");
 };
 
-__device__ __forceinline__ void record_status(int32_t* status, int code, int detail) {
-  if (atomicCAS(status, 0, code) == 0) {
-    status[1] = detail;
-    status[2] = (int)blockIdx.x;
-  }
-}
-
-// Waits on an mbarrier phase; gives up at the deadline or once any role has
-// raised the CTA-wide abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int* abort_any) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (*abort_any) return false;
-    if (globaltimer() - t0 > limit_ns) return false;
-  }
-}
-
-__device__ __forceinline__ float load_scale(const void* s, int kind, int idx) {
-  if (kind == PA_SCALE_GLOBAL) return reinterpret_cast<const float*>(s)[0];
-  return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(s)[idx]);
-}
-
-struct Item {
-  int b, kvh, tok0, ntok, cbase, kv0, kv1, chunk, nch, ntiles;
-};
-
-__device__ __forceinline__ Item load_item(const int32_t* items, int it) {
-  const int4* r = reinterpret_cast<const int4*>(items + (int64_t)it * kItemWords);
-  const int4 a = r[0], c = r[1];
-  Item m;
-  m.b = a.x; m.kvh = a.y; m.tok0 = a.z; m.ntok = a.w;
-  m.cbase = c.x; m.kv0 = c.y; m.kv1 = c.z; m.chunk = c.w & 0xFFFF; m.nch = c.w >> 16;
-  m.ntiles = (m.kv1 - m.kv0 + kTileTok - 1) / kTileTok;
-  return m;
-}
-
-// %globaltimer stamp of pipeline event `ev` of tile g (diagnostic trace)
-__device__ __forceinline__ void trace_ev(const AttnParams& p, uint32_t g, int ev) {
-  if (p.trace != nullptr && (int)blockIdx.x < p.trace_ctas && (int)g < p.trace_tiles)
-    p.trace[((int64_t)blockIdx.x * p.trace_tiles + g) * 16 + ev] = globaltimer();
-}
-
-// lane-0 arrive after the whole warp finished its part
-__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar);
-}
-
 // Walks the (item, tile) sequence of one CTA.
 struct TileCursor {
   int it, end, i, ntiles;
@@ -144,14 +92,14 @@ struct TileCursor {
     it = begin;
     end = e;
     i = 0;
-    ntiles = it < end ? load_item(items, it).ntiles : 0;
+    ntiles = it < end ? load_item<kTileTok>(items, it).ntiles : 0;
   }
   __device__ __forceinline__ bool valid() const { return it < end; }
   __device__ __forceinline__ void advance() {
     if (++i >= ntiles) {
       ++it;
       i = 0;
-      ntiles = it < end ? load_item(items, it).ntiles : 0;
+      ntiles = it < end ? load_item<kTileTok>(items, it).ntiles : 0;
     }
   }
 };
@@ -237,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued_g[s] = -1;
       bool ok = true;
       for (int it = item_begin; it < item_end && ok; ++it) {
-        const Item m = load_item(p.items, it);
+        const Item m = load_item<kTileTok>(p.items, it);
         const int32_t* bt = p.block_table + (int64_t)m.b * p.max_blocks;
         for (int t = 0; t < m.ntiles; ++t, ++g) {
           const int stage = g % kStages;
@@ -365,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O^T row d = this thread's TMEM lane, times 1/l and the V scale
     auto epilogue = [&](int li, uint32_t gl) -> bool {
       const int it = item_begin + li;
-      const Item m = load_item(p.items, it);
+      const Item m = load_item<kTileTok>(p.items, it);
       if (!wait_or_abort(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
         note_fail(it);
         return false;
@@ -410,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     float l[NH];
     for (int it = item_begin; it < item_end && !stop; ++it) {
-      const Item cur = load_item(p.items, it);
+      const Item cur = load_item<kTileTok>(p.items, it);
       const int li = it - item_begin;
       const int n_rows = cur.ntok * G;
       const float c_log2 = p.sm_scale_log2 *
@@ -633,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
     };
     for (int it = item_begin; it < item_end && !fail; ++it) {
-      const Item m = load_item(p.items, it);
+      const Item m = load_item<kTileTok>(p.items, it);
       const int li = it - item_begin;
       for (int i = 0; i < m.ntiles; ++i, ++g) {
         const int stage = g % kStages;

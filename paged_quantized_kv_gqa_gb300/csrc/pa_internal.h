@@ -91,6 +91,7 @@ struct AttnParams {
   int32_t scale_kind;
   int32_t max_chunks;
   int32_t skip_first_load;
+  int32_t q_box_tokens;  // query tokens per TMA box of the item's Q rows (append)
   float sm_scale_log2;   // sm_scale * log2(e)
   uint64_t* trace;       // [trace_ctas][trace_tiles][16] %globaltimer stamps, or null
   int32_t trace_ctas;
@@ -102,6 +103,8 @@ void set_error(const std::string& msg);
 // launchers (return a cudaError_t from the launch)
 cudaError_t launch_decode(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, cudaStream_t stream);
+cudaError_t launch_append(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
+                          const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream);
 cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
                          cudaStream_t stream);
 cudaError_t launch_gather(const pa_problem& prob, const pa_args& a, int32_t b, int32_t kvh,
