@@ -6,9 +6,11 @@ plan already uploaded and every input resident in HBM.  The default workload is
 decode-2 (bsz 64, q_len 1, 32 q heads / 8 kv heads, head dim 128, int8
 per-channel scales, prefix U[512, 4096], 4096-page shuffled pool, chunk 512);
 the metric is algorithmic KV-cache bytes (every visible (page, head) slab read
-once) per second.  --config 4 runs spec-verify-4 (same metric).
+once) per second.  --config 4 runs spec-verify-4 (same metric); --config 3 runs
+append-3 (chunked prefill, fp8 per-head, causal), whose metric is algorithmic
+FLOP/s (4 * D per visible (query head, position) pair) against the tensor peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|4] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4] [--impl reference]
 
 Prints one JSON line.  For N > 1 it runs under torch.distributed (one process
 per GPU); each rank runs an independent replica of the workload (the path has
@@ -34,13 +36,21 @@ METRIC = "KV-cache HBM GB/s (decode) & TFLOP/s (append/MLA), % of GB300 roofline
 L2_FLUSH_BYTES = 512 << 20
 
 
-def _peaks():
+def _peaks(bound: str):
+    """(peak, source) for an HBM-bound (GB/s) or tensor-bound (TFLOP/s) kernel.
+    The fp16 kind::f16 tensor rate equals the bf16 one the peaks file measures."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key, fallback = ("hbm_gbs", 6800.0) if bound == "hbm" else ("bf16_tflops", 1900.0)
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return float(d.get("hbm_gbs", 6800.0)), "measured"
-    return 6800.0, "fallback"
+        if key in d:
+            return float(d[key]), f"measured {key}"
+    return fallback, f"fallback {key}"
+
+
+def _is_flops_workload(config: int) -> bool:
+    return config in (3, 5)
 
 
 def _dist():
@@ -185,10 +195,14 @@ def run_cuda(args) -> dict:
     ms = statistics.mean(step_ms)
     ms_max = _max_over_ranks(ms, world)
     kv_bytes = desc["kv_bytes"]
-    value = kv_bytes * world / (ms_max * 1e-3) / 1e9
+    flops_mode = _is_flops_workload(args.config)
+    # work per step in the metric's unit (GB or TFLOP)
+    work, unit, bound, runit = ((desc["flops"] / 1e12, "TFLOP/s", "tensor", "TFLOP/s")
+                                if flops_mode else (kv_bytes / 1e9, "GB/s", "hbm", "GB/s"))
+    value = work * world / (ms_max * 1e-3)
     run_mean = statistics.mean(run_ms)
-    peak, peak_kind = _peaks()
-    achieved = kv_bytes / (run_mean * 1e-3) / 1e9
+    peak, peak_kind = _peaks(bound)
+    achieved = work / (run_mean * 1e-3)
     st, det = pa.pa_check(plan, ws, stream)
     if st != 0:
         raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
@@ -217,29 +231,30 @@ def run_cuda(args) -> dict:
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms.append(a.elapsed_time(b))
-    e2e = kv_bytes * world / (_max_over_ranks(statistics.mean(e2e_ms), world) * 1e-3) / 1e9
+    e2e = work * world / (_max_over_ranks(statistics.mean(e2e_ms), world) * 1e-3)
 
     res = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp16 (int8 KV dequantised exactly; fp32 accumulate)", "data": "synthetic",
+        "dtype": "fp16 (int8 / e4m3 KV dequantised exactly; fp32 accumulate)", "data": "synthetic",
         "config": {"workload": case.name, "desc": synth_desc(args.config),
-                   "kv_bytes_per_step": kv_bytes, "items": desc["num_items"],
+                   "kv_bytes_per_step": kv_bytes, "flops_per_step": desc["flops"],
+                   "items": desc["num_items"],
                    "ctas": desc["num_ctas"], "chunk": desc["chunk"],
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
-                     "peak_source": f"{peak_kind} hbm_gbs", "kernel": "pa_run attention kernel",
+        "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak,
+                     "unit": runit, "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": peak_kind, "kernel": "pa_run attention kernel",
                      "run_ms": round(run_mean, 5)},
-        "e2e": {"value": round(e2e, 2), "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
+        "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": K * (2 if split else 1),
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds, flops_mode)
     return res if rank == 0 else None
 
 
@@ -248,15 +263,22 @@ def synth_desc(n: int) -> str:
     return synth.CONFIG_NAMES[n]
 
 
-def cpu_baseline(case, seconds: float) -> dict:
+def cpu_baseline(case, seconds: float, flops_mode: bool = False) -> dict:
     """The fp64 oracle as it stands, on a bounded sample of (sequence, kv head) units."""
     from oracle import attention as oa
     units = [(b, h) for b in range(case.bsz) for h in range(case.kv_heads)]
     rng = np.random.default_rng(0)
     rng.shuffle(units)
     done_bytes = 0
-    per_unit = lambda b: int(np.ceil((case.seq_lens_kv[b] + case.seq_lens[b]) / case.block_size)) \
-        * case.block_size * (case.head_dim_qk + case.head_dim_v)
+    G = case.q_heads // case.kv_heads
+
+    def per_unit(b):
+        q, pre = float(case.seq_lens[b]), float(case.seq_lens_kv[b])
+        if flops_mode:   # visible (query head, position) pairs x 2 (Dqk + Dv)
+            pairs = q * pre + q * (q + 1) / 2 if case.causal else q * (pre + q)
+            return pairs * G * 2 * (case.head_dim_qk + case.head_dim_v)
+        return int(np.ceil((pre + q) / case.block_size)) * case.block_size \
+            * (case.head_dim_qk + case.head_dim_v)
     t0 = time.perf_counter()
     n = 0
     for b, h in units:
@@ -266,7 +288,9 @@ def cpu_baseline(case, seconds: float) -> dict:
         if time.perf_counter() - t0 > seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(done_bytes / dt / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+    per_s = done_bytes / dt / (1e12 if flops_mode else 1e9)
+    return {"value": round(per_s, 6), "unit": "TFLOP/s" if flops_mode else "GB/s",
+            "cores": 1, "kind": "oracle",
             "sample": f"{n} of {len(units)} (sequence, kv head) units of {case.name}, "
                       f"{dt:.1f} s, numpy fp64 (single-threaded gather/einsum)"}
 
@@ -278,19 +302,21 @@ def run_reference(args) -> dict:
     case = _workload(args.config)
     K, W = args.steps, args.warmup
     per = max(1.0, args.cpu_seconds / max(1, K + W))
+    flops_mode = _is_flops_workload(args.config)
     vals = []
     for i in range(W + K):
-        cb = cpu_baseline(case, per)
+        cb = cpu_baseline(case, per, flops_mode)
         if i >= W:
             vals.append(cb["value"])
     v = statistics.mean(vals)
     cb["value"] = round(v, 6)
-    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": "GB/s",
+    unit = cb["unit"]
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit,
             "n_gpus": 1, "steps": K, "warmup": W, "higher_is_better": True,
             "ms_per_step": None, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": case.name, "desc": synth_desc(args.config)},
             "cpu_baseline": cb,
-            "e2e": {"value": round(v, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+            "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
 
@@ -299,7 +325,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[2, 4])
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
