@@ -10,7 +10,7 @@ once) per second.  --config 4 runs spec-verify-4 (same metric); --config 3 runs
 append-3 (chunked prefill, fp8 per-head, causal), whose metric is algorithmic
 FLOP/s (4 * D per visible (query head, position) pair) against the tensor peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4] [--impl reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4|5] [--impl reference]
 
 Prints one JSON line.  For N > 1 it runs under torch.distributed (one process
 per GPU); each rank runs an independent replica of the workload (the path has
@@ -325,7 +325,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4])
+    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -178,7 +178,8 @@ pa_status pa_plan_upload(const pa_plan_t* plan, void* workspace, void* stream);
 
 /* Enqueues the attention kernel of the plan's family for every work item
  * (decode: q_len * G <= 64 packed rows per tile; append: 256 packed rows per
- * item, out must be 16-byte aligned).  Items that cover the whole KV range of
+ * item; MLA: one query token per item on a 2-CTA cluster; append and MLA need
+ * out 16-byte aligned).  Items that cover the whole KV range of
  * their rows write out/lse directly; split rows write partial states into the
  * workspace and need pa_merge afterwards.  The workspace must hold this plan
  * (pa_plan_upload).  PA_ERR_UNSUPPORTED for a family whose kernel is not

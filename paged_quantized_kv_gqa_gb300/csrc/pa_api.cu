@@ -288,14 +288,15 @@ static EncodeTiledFn get_encode() {
   return fn;
 }
 
-// 2-D byte tensor [rows][cols] with a box of [box_rows][cols].
+// 2-D byte tensor [rows][cols] with a box of [box_rows][box_cols] (whole rows
+// unless box_cols is given).
 static pa_status make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
-                          uint32_t box_rows, CUtensorMapSwizzle sw) {
+                          uint32_t box_rows, CUtensorMapSwizzle sw, uint32_t box_cols = 0) {
   EncodeTiledFn enc = get_encode();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled not available from the driver");
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {cols};
-  const cuuint32_t box[2] = {(cuuint32_t)cols, box_rows};
+  const cuuint32_t box[2] = {box_cols ? box_cols : (cuuint32_t)cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -473,7 +474,14 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
     p.q_box_tokens = box_tok;
     e = launch_append(*plan, p, tk, tv, tq, st);
   } else {
-    return fail(PA_ERR_UNSUPPORTED, "kernel family not built yet");
+    // MLA: one latent row of 576 bytes per position, read as 128-byte boxes
+    if (reinterpret_cast<uintptr_t>(args->out) % 16)
+      return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned");
+    CUtensorMap tc;
+    s = make_map(&tc, args->cache_k, (uint64_t)pr.num_pages * pr.block_size, pr.head_dim_qk, 64,
+                 CU_TENSOR_MAP_SWIZZLE_128B, 128);
+    if (s != PA_OK) return s;
+    e = launch_mla(*plan, p, tc, st);
   }
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("launch: ") + cudaGetErrorString(e));
   return PA_OK;

@@ -55,15 +55,13 @@ constexpr int kWarpTma = 12;
 constexpr int kWarpMma0 = 13;                    // issues the MMAs of query tile A
 constexpr int kWarpMma1 = 14;                    // ... of query tile B
 constexpr uint32_t kTmemCols = 512;
-constexpr int kCvBar = 3;                        // named barrier of the CV warpgroup
 
 struct Smem {
   static constexpr int kRaw = 0;                              // [kStages][K0 K1 V0 V1]
   static constexpr int kQ = kStages * kStageBytes;            // [2 k-halves][256 rows][128 B]
   static constexpr int kK16 = kQ + kRows * 256;               // [2][128 positions][128 B]
   static constexpr int kV16 = kK16 + kTile * 256;             // [2][128 dims][128 B]
-  static constexpr int kKsc = kV16 + kTile * 256;             // [128] fp32 per-channel K scale
-  static constexpr int kBars = kKsc + kHeadDim * 4;
+  static constexpr int kBars = kV16 + kTile * 256;
   // full[S] empty[S] qfull qready qfree kready kfree vready vfree sfull[2] pready[2] pvdone[2]
   static constexpr int kNumBars = 2 * kStages + 7 + 6;
   static constexpr int kMisc = kBars + kNumBars * 8;          // tmem address, abort flag
@@ -441,7 +439,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ================================================================ CV warpgroup
     const int t = tid & 127;          // K position / V head dim of the tile
-    float* ksc = reinterpret_cast<float*>(smem + SM::kKsc);
     uint32_t g = 0;
     bool fail = false;
     auto note_fail = [&](int it) {
@@ -453,12 +450,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item m = load_item<kTile>(p.items, it);
       const int li = it - item_begin;
       const bool pc = p.scale_kind == PA_SCALE_PER_CHANNEL;
-      const float sc_t = pc ? load_scale(p.k_scale, PA_SCALE_PER_CHANNEL, m.kvh * kHeadDim + t) : 1.0f;
+      const __nv_bfloat16* ksc =
+          reinterpret_cast<const __nv_bfloat16*>(p.k_scale) + m.kvh * kHeadDim;
       if (!wait_or_abort(qfull, li & 1, limit, abort_any)) { note_fail(it); break; }
       // Q' = bf16 Q (times the per-channel K scale) -> fp16, in place
-      bar_sync(kCvBar, 128);   // the previous item's conversion is done with ksc
-      ksc[t] = sc_t;
-      bar_sync(kCvBar, 128);
       for (int task = t; task < kRows * 16; task += 128) {
         const int row = task >> 4, ch = task & 15;
         const int kb = ch >> 3, cc = ch & 7;
@@ -467,9 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
         float f[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          f[e] = __bfloat162float(hv[e]);
-          if (pc) f[e] *= ksc[ch * 8 + e];
+        for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]);
+        if (pc) {
+          const uint4 sr = *reinterpret_cast<const uint4*>(ksc + ch * 8);
+          const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(&sr);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) f[e] *= __bfloat162float(sv[e]);
         }
         uint4 packed;
         packed.x = pack_half2(f[0], f[1]);

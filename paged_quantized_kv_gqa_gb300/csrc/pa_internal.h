@@ -105,6 +105,8 @@ cudaError_t launch_decode(const Plan& plan, const AttnParams& p, const CUtensorM
                           const CUtensorMap& tm_v, cudaStream_t stream);
 cudaError_t launch_append(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream);
+cudaError_t launch_mla(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_c,
+                       cudaStream_t stream);
 cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
                          cudaStream_t stream);
 cudaError_t launch_gather(const pa_problem& prob, const pa_args& a, int32_t b, int32_t kvh,

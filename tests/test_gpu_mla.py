@@ -1,0 +1,61 @@
+"""GPU parity of the MLA path (128 query heads over one latent head, K 576 /
+V 512, global scale) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+
+import synth
+from gpu_helpers import run_case, compare
+
+pytestmark = pytest.mark.gpu
+
+MLA = dict(q_heads=128, kv_heads=1, head_dim_qk=576, head_dim_v=512, layout="mla",
+           scale_kind="global", sm_scale=1.0 / np.sqrt(192.0))
+
+
+def _mla_case(seed, **kw):
+    args = dict(MLA)
+    args.setdefault("kv_dtype", "fp8_e4m3")
+    args.update(kw)
+    return synth.make_case(name="mla-edge", seed=seed, **args)
+
+
+EDGE = [
+    # kv ranges around page boundaries, one token each, no split
+    dict(seq_lens=[1, 1, 1, 1], seq_lens_kv=[0, 63, 64, 200], chunk_size=0),
+    # two tokens (causal between them), split with merge
+    dict(seq_lens=[2, 1, 2], seq_lens_kv=[700, 1000, 129], chunk_size=256),
+    # planner's automatic chunk size
+    dict(seq_lens=[1, 2], seq_lens_kv=[3000, 2500], chunk_size=-1),
+    # int8 latent cache with a global scale
+    dict(seq_lens=[2, 1], seq_lens_kv=[333, 64], chunk_size=128, kv_dtype="int8"),
+    # non-causal
+    dict(seq_lens=[2], seq_lens_kv=[190], chunk_size=0, causal=False),
+]
+
+
+@pytest.mark.parametrize("kw", EDGE)
+def test_mla_edge_cases(kw):
+    case = _mla_case(21, **kw)
+    out, lse, plan, _, _ = run_case(case)
+    assert plan.describe()["family"] == "mla"
+    compare(case, out, lse, label=str(kw))
+
+
+def test_mla_5_sampled():
+    """Full-size MLA workload (bsz 32, q_len U{1,2}, prefix U[4096,16384], fp8
+    global scale, automatic split + merge) in the benchmark's launch
+    configuration; the oracle checks a spread of sequences."""
+    case = synth.config(5)
+    out, lse, plan, _, _ = run_case(case)
+    d = plan.describe()
+    assert d["family"] == "mla" and d["max_chunks"] > 1
+    bs = sorted(set(np.random.default_rng(0).choice(case.bsz, 6, replace=False).tolist())
+                | {0, case.bsz - 1})
+    compare(case, out, lse, units=[(b, 0) for b in bs], label="mla-5")
+
+
+def test_mla_repeat_bitexact():
+    case = _mla_case(22, seq_lens=[2, 1], seq_lens_kv=[900, 50], chunk_size=256)
+    out1, lse1, _, d, _ = run_case(case)
+    out2, lse2, _, _, _ = run_case(case, d=d)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
