@@ -49,6 +49,32 @@ def _peaks(bound: str):
     return fallback, f"fallback {key}"
 
 
+# DRAM bytes (read + written) per launch of each attention kernel, from one
+# `ncu --set full` capture (summaries under profiles/).  A figure is reported
+# only while the kernel source still hashes to the version it was taken with.
+NCU_TRAFFIC = {
+    "decode-2": ("pa_decode.cu", "3a7c273e7c0864e5", 319.308032e6 + 4.890368e6),
+    "append-3": ("pa_append.cu", "388089fb01ca7b40", 72.266496e6 + 2.511104e6),
+    "mla-5": ("pa_mla.cu", "1b3ae6c0e072d3f4", 199.242752e6 + 23.372288e6),
+}
+
+
+def _kernel_sha(fname: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for n in (fname, "pa_common.cuh", "pa_ptx.cuh"):
+        with open(os.path.join(ROOT, "paged_quantized_kv_gqa_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload: str):
+    ent = NCU_TRAFFIC.get(workload)
+    if ent is None or _kernel_sha(ent[0]) != ent[1]:
+        return None
+    return int(ent[2])
+
+
 def _is_flops_workload(config: int) -> bool:
     return config in (3, 5)
 
@@ -63,14 +89,22 @@ def _dist():
     return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
-def _max_over_ranks(x: float, world: int) -> float:
+def _max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
+    """Largest per-rank value (the step time the job is charged): NCCL on the
+    GPUs, gloo on the host."""
     if world <= 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def _job_rate(work_per_rank: float, world: int, ms_max: float) -> float:
+    """Whole-job throughput of N independent replicas: every rank's work over
+    the slowest rank's time (weak scaling)."""
+    return work_per_rank * world / (ms_max * 1e-3)
 
 
 def _barrier(world: int):
@@ -199,7 +233,7 @@ def run_cuda(args) -> dict:
     # work per step in the metric's unit (GB or TFLOP)
     work, unit, bound, runit = ((desc["flops"] / 1e12, "TFLOP/s", "tensor", "TFLOP/s")
                                 if flops_mode else (kv_bytes / 1e9, "GB/s", "hbm", "GB/s"))
-    value = work * world / (ms_max * 1e-3)
+    value = _job_rate(work, world, ms_max)
     run_mean = statistics.mean(run_ms)
     peak, peak_kind = _peaks(bound)
     achieved = work / (run_mean * 1e-3)
@@ -231,7 +265,7 @@ def run_cuda(args) -> dict:
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms.append(a.elapsed_time(b))
-    e2e = work * world / (_max_over_ranks(statistics.mean(e2e_ms), world) * 1e-3)
+    e2e = _job_rate(work, world, _max_over_ranks(statistics.mean(e2e_ms), world))
 
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
@@ -245,7 +279,8 @@ def run_cuda(args) -> dict:
                    "l2": "flushed (512 MiB write) before every timed step",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": runit, "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": runit, "frac": round(achieved / peak, 4),
+                     "traffic": _traffic(case.name), "traffic_unit": "bytes per launch (ncu)",
                      "peak_source": peak_kind, "kernel": "pa_run attention kernel",
                      "run_ms": round(run_mean, 5)},
         "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": int(h2d),
