@@ -10,29 +10,31 @@
 // mma.sync, dequantisation inside the MMA fragments) is replaced by:
 //
 //   * Rows as M.  An item holds 256 packed rows, two 128-row query tiles A
-//     and B that share every K/V tile.  Per 128-position KV tile and query
-//     tile: S = Q' K^T is one 128x128 fp32 accumulator in TMEM (8 x
-//     tcgen05.mma, K = 16 each); P (fp16) overwrites S in TMEM and is the TMEM
-//     A operand of O += P V (8 more MMAs), O being 128x128 fp32 in TMEM.
-//     TMEM: S_A 0, S_B 128, O_A 256, O_B 384 (all 512 columns).
+//     and B that share every K/V tile.  KV tiles are one 64-position page:
+//     per tile and query tile, S = Q' K^T is a 128 x 64 fp32 accumulator in
+//     TMEM (8 tcgen05.mma, N 64, K 16 each); P (fp16) overwrites S in TMEM and
+//     is the TMEM A operand of O += P V (4 MMAs, N 128), O being 128 x 128
+//     fp32 in TMEM.  TMEM: S_A[2] 0/64, S_B[2] 128/192, O_A 256, O_B 384.
+//   * S is double-buffered per query tile, so S of the next page is computed
+//     while the softmax works on the current one and the softmax finds it
+//     waiting.
 //   * One persistent CTA of four warpgroups per SM:
-//       SM_A, SM_B  softmax of query tile A / B, thread = row: exact row max
-//                   of the tile, lazy rescale (threshold 2^8) of l and of the
-//                   thread's O row in TMEM, P into TMEM, epilogue of its row;
+//       SM_A, SM_B  softmax of query tile A / B, thread = row: the 64 scores of
+//                   a page in one TMEM load, lazy rescale (threshold 2^8) of l
+//                   and of the thread's O row, P into TMEM, epilogue of its row;
 //       CV          Q' (bf16 -> fp16 times the per-channel K scale, in place)
-//                   and the K / V tiles, int8 or e4m3 -> fp16 (exact), into
-//                   128B-swizzled K-major shared memory: K as the B operand of
-//                   S (rows = positions), V^T as the B operand of PV (rows =
-//                   head dims, which is the cache's own V layout);
+//                   and each page's K / V, int8 or e4m3 -> fp16 (exact), into
+//                   double-buffered 128B-swizzled K-major shared memory: K as
+//                   the B operand of S (rows = positions), V^T as the B operand
+//                   of PV (rows = head dims, which is the cache's own V layout);
 //       IO          one TMA warp (the item's Q rows as a 3-D box, K and V page
-//                   slabs into a 3-stage ring) and two MMA-issue warps, one
-//                   per query tile, so each tile's S -> softmax -> PV chain
-//                   runs independently and the tensor pipe interleaves them.
-//   * Ordering rules that make the single-buffered S/P, K16, V16 and Q' safe:
-//     S_X(t) is issued only after PV_X(t-1) completed (P_X is read by it, and
-//     O_X is then quiescent for the softmax's rescale), K16 / V16 / Q' are
-//     rewritten only after both chains' MMAs that read them completed
-//     (tcgen05.commit to two-arrival barriers).
+//                   slabs into a 4-stage ring) and two MMA-issue warps: one
+//                   issues S of both query tiles (up to two pages ahead), the
+//                   other PV, so neither waits behind the other's MMAs.
+//   * Ordering rules: S_X into buffer b waits for the PV_X that read P_X from b;
+//     the softmax rescales O_X only after the PV_X of the previous page
+//     completed; K16 / V16 buffer b and Q' are rewritten only after the
+//     MMAs that read them completed (tcgen05.commit of the issuing thread).
 //   * Per-kv-head / global K scales fold into the softmax scale, V scales into
 //     the epilogue, per-channel K scales into Q'.
 #include <cfloat>
@@ -42,35 +44,38 @@
 namespace pa {
 namespace {
 
-constexpr int kTile = 128;                       // KV positions per tile
+constexpr int kTile = 64;                        // KV positions per tile (one page)
 constexpr int kHeadDim = 128;
 constexpr int kPage = 64;
 constexpr int kRows = 256;                       // packed query rows per item
 constexpr int kSlab = kPage * kHeadDim;          // bytes of one (page, head) K or V slab
-constexpr int kStageBytes = 4 * kSlab;           // K (2 pages) + V (2 pages)
-constexpr int kStages = 3;
+constexpr int kStageBytes = 2 * kSlab;           // K slab + V slab
+constexpr int kStages = 4;
+constexpr int kK16Bytes = kTile * 256;           // [2 dim halves][64 positions][128 B]
+constexpr int kV16Bytes = kHeadDim * 128;        // [128 dims][64 positions x 2 B]
 constexpr float kTau = 8.0f;                     // lazy-rescale threshold (log2 units)
 constexpr int kThreads = 512;
 constexpr int kWarpTma = 12;
-constexpr int kWarpMma0 = 13;                    // issues the MMAs of query tile A
-constexpr int kWarpMma1 = 14;                    // ... of query tile B
+constexpr int kWarpMmaS = 13;                    // issues S = Q' K^T of both query tiles
+constexpr int kWarpMmaPV = 14;                   // issues O += P V of both query tiles
 constexpr uint32_t kTmemCols = 512;
 
 struct Smem {
-  static constexpr int kRaw = 0;                              // [kStages][K0 K1 V0 V1]
+  static constexpr int kRaw = 0;                              // [kStages][K slab | V slab]
   static constexpr int kQ = kStages * kStageBytes;            // [2 k-halves][256 rows][128 B]
-  static constexpr int kK16 = kQ + kRows * 256;               // [2][128 positions][128 B]
-  static constexpr int kV16 = kK16 + kTile * 256;             // [2][128 dims][128 B]
-  static constexpr int kBars = kV16 + kTile * 256;
-  // full[S] empty[S] qfull qready qfree kready kfree vready vfree sfull[2] pready[2] pvdone[2]
-  static constexpr int kNumBars = 2 * kStages + 7 + 6;
+  static constexpr int kK16 = kQ + kRows * 256;               // [2 buffers]
+  static constexpr int kV16 = kK16 + 2 * kK16Bytes;           // [2 buffers]
+  static constexpr int kBars = kV16 + 2 * kV16Bytes;
+  // full[S] empty[S] qfull qready qfree kready[2] kfree[2] vready[2] vfree[2]
+  // sfull[2][2] pready[2][2] pvdone[2][2] drain[2]
+  static constexpr int kNumBars = 2 * kStages + 3 + 8 + 12 + 2;
   static constexpr int kMisc = kBars + kNumBars * 8;          // tmem address, abort flag
   static constexpr int kTotal = kMisc + 16 + 1024;            // + alignment slack
   static_assert(kTotal <= 232448, "shared memory overflow");
 };
 
 // Shared-memory descriptor of k-step kk (16 elements) of a K-major SW128
-// operand whose two 64-element halves are `half_bytes` apart.
+// operand whose 64-element halves are `half_bytes` apart.
 __device__ __forceinline__ uint64_t kstep_desc(uint32_t base, int kk, int half_bytes) {
   return sdesc_k128(base + (kk >> 2) * half_bytes + (kk & 3) * 32);
 }
@@ -91,13 +96,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* qfull = empty + kStages;
   uint64_t* qready = qfull + 1;
   uint64_t* qfree = qready + 1;
-  uint64_t* kready = qfree + 1;
-  uint64_t* kfree = kready + 1;
-  uint64_t* vready = kfree + 1;
-  uint64_t* vfree = vready + 1;
-  uint64_t* sfull = vfree + 1;     // [2]
-  uint64_t* pready = sfull + 2;    // [2]
-  uint64_t* pvdone = pready + 2;   // [2]
+  uint64_t* kready = qfree + 1;    // [2] by K16 buffer
+  uint64_t* kfree = kready + 2;    // [2]
+  uint64_t* vready = kfree + 2;    // [2] by V16 buffer
+  uint64_t* vfree = vready + 2;    // [2]
+  uint64_t* sfull = vfree + 2;     // [query tile][S buffer]
+  uint64_t* pready = sfull + 4;    // [query tile][S buffer]
+  uint64_t* pvdone = pready + 4;   // [query tile][S buffer]
+  uint64_t* drain = pvdone + 4;    // [S issuer, PV issuer]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
   volatile int* abort_any = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
   const uint32_t s_base = smem_u32(smem);
@@ -121,15 +127,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(qfull, 1);
     mbar_init(qready, 4);
-    mbar_init(qfree, 2);
-    mbar_init(kready, 4);
-    mbar_init(kfree, 2);
-    mbar_init(vready, 4);
-    mbar_init(vfree, 2);
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(&sfull[x], 1);
-      mbar_init(&pready[x], 4);
-      mbar_init(&pvdone[x], 1);
+    mbar_init(qfree, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&kready[b], 4);
+      mbar_init(&kfree[b], 1);
+      mbar_init(&vready[b], 4);
+      mbar_init(&vfree[b], 1);
+      mbar_init(&drain[b], 1);
+    }
+    for (int j = 0; j < 4; ++j) {
+      mbar_init(&sfull[j], 1);
+      mbar_init(&pready[j], 4);
+      mbar_init(&pvdone[j], 1);
     }
     *abort_any = 0;
     fence_mbar_init();
@@ -173,11 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < m.ntiles; ++t, ++g) {
           const int stage = g % kStages;
           const uint32_t ph = (g / kStages) & 1;
-          const int pos0 = m.kv0 + t * kTile;
-          const int npg = (m.kv1 - pos0) > kPage ? 2 : 1;
-          int pages[2];
-          pages[0] = bt[pos0 / kPage];
-          pages[1] = npg == 2 ? bt[pos0 / kPage + 1] : 0;
+          const int page = bt[(m.kv0 + t * kTile) / kPage];
           if (!wait_or_abort(&empty[stage], ph ^ 1, limit, abort_any)) {
             if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
             *abort_any = 1;
@@ -185,23 +190,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           if (p.skip_first_load && g == 0) continue;  // failure-detection test hook
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)(npg * 2 * kSlab));
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)(2 * kSlab));
           issued_g[stage] = (int)g;
           uint8_t* st = smem + SM::kRaw + stage * kStageBytes;
-          for (int pg = 0; pg < npg; ++pg) {
-            const int page = pages[pg];
-            int yk, yv;
-            if (page < 0 || page >= p.num_pages) {
-              record_status(p.status, PA_ERR_BAD_PAGE, it);
-              yk = p.num_pages * p.kv_heads * kPage;       // past the end: TMA fills zeros
-              yv = p.num_pages * p.kv_heads * kHeadDim;
-            } else {
-              yk = (page * p.kv_heads + m.kvh) * kPage;
-              yv = (page * p.kv_heads + m.kvh) * kHeadDim;
-            }
-            tma_load_2d(st + pg * kSlab, &tm_k, &full[stage], 0, yk);
-            tma_load_2d(st + 2 * kSlab + pg * kSlab, &tm_v, &full[stage], 0, yv);
+          int yk, yv;
+          if (page < 0 || page >= p.num_pages) {
+            record_status(p.status, PA_ERR_BAD_PAGE, it);
+            yk = p.num_pages * p.kv_heads * kPage;       // past the end: TMA fills zeros
+            yv = p.num_pages * p.kv_heads * kHeadDim;
+          } else {
+            yk = (page * p.kv_heads + m.kvh) * kPage;
+            yv = (page * p.kv_heads + m.kvh) * kHeadDim;
           }
+          tma_load_2d(st, &tm_k, &full[stage], 0, yk);
+          tma_load_2d(st + kSlab, &tm_v, &full[stage], 0, yv);
+          trace_ev(p, g, 0);
         }
       }
       // every issued load lands before the CTA exits
@@ -209,51 +212,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, limit);
       if (q_issued > 0) mbar_wait(qfull, (q_issued - 1) & 1, limit);
     }
-  } else if (warp == kWarpMma0 || warp == kWarpMma1) {
-    // ================================================================ MMA issue
-    // chain X: S_X(t) = Q'_X K16^T, then O_X += P_X V16, tile after tile
+  } else if (warp == kWarpMmaS) {
+    // ================================================================ S issue
+    // S_X = Q'_X K16^T for both query tiles, into S buffer (chain tile) & 1;
+    // runs up to two pages ahead of the PV issue
     if (lane == 0) {
-      const int X = warp - kWarpMma0;
-      const uint32_t idesc = idesc_f16_f32(128, 128);
-      const uint32_t s_tm = tmem + X * 128;
-      const uint32_t o_tm = tmem + 256 + X * 128;
-      const uint32_t qa = q_s + X * 128 * 128;
-      uint32_t g = 0, gx = 0, n_s = 0;
+      const uint32_t idesc_s = idesc_f16_f32(128, kTile);
+      uint32_t g = 0, gx[2] = {0, 0};
       bool ok = true;
       for (int it = item_begin; it < item_end && ok; ++it) {
         const Item m = load_item<kTile>(p.items, it);
         const int li = it - item_begin;
-        const bool active = X == 0 || m.ntok * G > 128;
+        const int nq = m.ntok * G > 128 ? 2 : 1;   // query tiles holding rows
         if (!wait_or_abort(qready, li & 1, limit, abort_any)) { ok = false; break; }
-        for (int i = 0; i < m.ntiles; ++i, ++g) {
-          if (!wait_or_abort(kready, g & 1, limit, abort_any)) { ok = false; break; }
-          if (active) {
-            if (gx > 0 && !wait_or_abort(&pvdone[X], (gx - 1) & 1, limit, abort_any)) {
+        for (int i = 0; i < m.ntiles && ok; ++i, ++g) {
+          if (!wait_or_abort(&kready[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
+          const uint32_t kb = k16 + (g & 1) * kK16Bytes;
+          for (int X = 0; X < nq; ++X) {
+            const uint32_t gs = gx[X];
+            // S buffer gs&1 held P of this tile's page gs-2: its PV must be done
+            if (gs >= 2 &&
+                !wait_or_abort(&pvdone[2 * X + (gs & 1)], ((gs - 2) >> 1) & 1, limit, abort_any)) {
               ok = false;
               break;
             }
             tc_fence_after();
+            const uint32_t s_tm = tmem + X * 128 + (gs & 1) * kTile;
+            const uint32_t qa = q_s + X * 128 * 128;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(s_tm, kstep_desc(qa, kk, kRows * 128), kstep_desc(k16, kk, kTile * 128), idesc,
-                     kk > 0 ? 1u : 0u);
-            tc_commit(&sfull[X]);
-            ++n_s;
+              mma_ss(s_tm, kstep_desc(qa, kk, kRows * 128), kstep_desc(kb, kk, kTile * 128),
+                     idesc_s, kk > 0 ? 1u : 0u);
+            tc_commit(&sfull[2 * X + (gs & 1)]);
+            gx[X] = gs + 1;
           }
-          tc_commit(kfree);
+          if (!ok) break;
+          tc_commit(&kfree[g & 1]);
           if (i + 1 == m.ntiles) tc_commit(qfree);
-          if (!wait_or_abort(vready, g & 1, limit, abort_any)) { ok = false; break; }
-          if (active) {
-            if (!wait_or_abort(&pready[X], gx & 1, limit, abort_any)) { ok = false; break; }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(o_tm, s_tm + 8 * kk, kstep_desc(v16, kk, kTile * 128), idesc,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&pvdone[X]);
-            ++gx;
-          }
-          tc_commit(vfree);
+          trace_ev(p, g, 8);
         }
       }
       if (!ok) {
@@ -261,8 +257,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_any = 1;
       }
       // drain: every MMA this thread issued completes before TMEM is released
-      if (n_s > 0) mbar_wait(&sfull[X], (n_s - 1) & 1, limit);
-      if (gx > 0) mbar_wait(&pvdone[X], (gx - 1) & 1, limit);
+      tc_commit(&drain[0]);
+      mbar_wait(&drain[0], 0, limit);
+    }
+  } else if (warp == kWarpMmaPV) {
+    // ================================================================ PV issue
+    // O_X += P_X V16 for both query tiles, P_X read from TMEM (A operand)
+    if (lane == 0) {
+      const uint32_t idesc_pv = idesc_f16_f32(128, kHeadDim);
+      uint32_t g = 0, gx[2] = {0, 0};
+      bool ok = true;
+      for (int it = item_begin; it < item_end && ok; ++it) {
+        const Item m = load_item<kTile>(p.items, it);
+        const int nq = m.ntok * G > 128 ? 2 : 1;
+        for (int i = 0; i < m.ntiles && ok; ++i, ++g) {
+          if (!wait_or_abort(&vready[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
+          const uint32_t vb = v16 + (g & 1) * kV16Bytes;
+          for (int X = 0; X < nq; ++X) {
+            const uint32_t gp = gx[X];
+            if (!wait_or_abort(&pready[2 * X + (gp & 1)], (gp >> 1) & 1, limit, abort_any)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t p_tm = tmem + X * 128 + (gp & 1) * kTile;
+            const uint32_t o_tm = tmem + 256 + X * 128;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(o_tm, p_tm + 8 * kk, sdesc_k128(vb + kk * 32), idesc_pv,
+                     (i > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&pvdone[2 * X + (gp & 1)]);
+            gx[X] = gp + 1;
+          }
+          if (!ok) break;
+          tc_commit(&vfree[g & 1]);
+          trace_ev(p, g, 9);
+        }
+      }
+      if (!ok) {
+        if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
+        *abort_any = 1;
+      }
+      tc_commit(&drain[1]);
+      mbar_wait(&drain[1], 0, limit);
     }
   } else if (wg == 3) {
     // warp 15: no role (it completes the fourth warpgroup)
@@ -272,13 +309,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int X = wg;
     const int rr = tid & 127;
     const int r = X * 128 + rr;
-    const uint32_t s_tm = t_lane + X * 128;
     const uint32_t o_tm = t_lane + 256 + X * 128;
-    uint32_t gx = 0;
+    uint64_t* my_sfull = sfull + 2 * X;
+    uint64_t* my_pready = pready + 2 * X;
+    uint64_t* my_pvdone = pvdone + 2 * X;
+    uint32_t gx = 0, gg = 0;   // tiles of this query tile / of the CTA (trace only)
     bool fail = false;
+    auto note_fail = [&](int it) {
+      if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
+      *abort_any = 1;
+      fail = true;
+    };
     for (int it = item_begin; it < item_end && !fail; ++it) {
       const Item m = load_item<kTile>(p.items, it);
-      if (!(X == 0 || m.ntok * G > 128)) continue;   // tile B holds no rows of this item
+      if (!(X == 0 || m.ntok * G > 128)) {   // tile B holds no rows of this item
+        gg += m.ntiles;
+        continue;
+      }
       const int n_rows = m.ntok * G;
       const bool row_ok = r < n_rows;
       const int tok = r / G;
@@ -288,31 +335,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       // causal base, or kvtot without a causal mask)
       const int vis_lim = min(m.kv1, m.cbase + tok + 1);
       float m_run = -INFINITY, l = 0.0f;
-      for (int i = 0; i < m.ntiles; ++i, ++gx) {
-        if (!wait_or_abort(&sfull[X], gx & 1, limit, abort_any)) {
-          if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
-          *abort_any = 1;
-          fail = true;
+      for (int i = 0; i < m.ntiles; ++i, ++gx, ++gg) {
+        if (!wait_or_abort(&my_sfull[gx & 1], (gx >> 1) & 1, limit, abort_any)) {
+          note_fail(it);
           break;
         }
         tc_fence_after();
+        if (rr == 0) trace_ev(p, gg, X ? 12 : 3);
+        const uint32_t s_tm = t_lane + X * 128 + (gx & 1) * kTile;
+        uint32_t v[64];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld16(s_tm + 16 * c, *reinterpret_cast<uint32_t(*)[16]>(&v[16 * c]));
+        tmem_wait_ld();
         const int nvis = max(0, min(kTile, vis_lim - (m.kv0 + i * kTile)));
-        // ---- pass 1: maximum of the visible raw scores
+        const bool full_tile = nvis == kTile;
         float mx = -INFINITY;
+        if (full_tile) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t v[32];
-          tmem_ld16(s_tm + 32 * q4, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-          tmem_ld16(s_tm + 32 * q4 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-          tmem_wait_ld();
-          if (nvis >= 32 * q4 + 32) {
+          for (int e = 0; e < 64; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
+        } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(v[e]));
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (32 * q4 + e < nvis) mx = fmaxf(mx, __uint_as_float(v[e]));
-          }
+          for (int e = 0; e < 64; ++e)
+            if (e < nvis) mx = fmaxf(mx, __uint_as_float(v[e]));
         }
         const float m_tile = mx * c_log2;   // log2 units; -inf when nothing is visible
         const bool need = m_tile > m_run + kTau;
@@ -322,63 +367,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           l *= alpha;
           m_run = m_tile;
         }
-        // O_X holds the PV of earlier tiles of this item: rescale this row.
-        // PV_X of the previous tile completed before S_X of this one was issued.
+        // O_X holds the PV of earlier pages of this item: once the last of them
+        // completed, rescale this row (rare after the first pages)
         if (i > 0 && __any_sync(0xffffffffu, need)) {
-#pragma unroll
+          if (!wait_or_abort(&my_pvdone[(gx - 1) & 1], ((gx - 1) >> 1) & 1, limit, abort_any)) {
+            note_fail(it);
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 2
           for (int c = 0; c < 8; ++c) {
-            uint32_t v[16];
-            tmem_ld16(o_tm + 16 * c, v);
+            uint32_t o[16];
+            tmem_ld16(o_tm + 16 * c, o);
             tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tmem_st16(o_tm + 16 * c, v);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st16(o_tm + 16 * c, o);
           }
-          tmem_wait_st();
         }
-        // ---- pass 2: P = 2^(s c - m) over the visible positions, written as
-        // fp16 over the S columns already consumed
+        // P = 2^(s c - m) over the visible positions, fp16, over the S columns
         const float neg_m = m_run == -INFINITY ? 0.0f : -m_run;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint32_t v[32];
-          tmem_ld16(s_tm + 32 * q4, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
-          tmem_ld16(s_tm + 32 * q4 + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
-          tmem_wait_ld();
+        for (int h = 0; h < 2; ++h) {
           uint32_t w[16];
-          if (nvis >= 32 * q4 + 32) {
+          if (full_tile) {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(v[2 * e]), c_log2, neg_m));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c_log2, neg_m));
+              const float p0 = fast_exp2(fmaf(__uint_as_float(v[32 * h + 2 * e]), c_log2, neg_m));
+              const float p1 =
+                  fast_exp2(fmaf(__uint_as_float(v[32 * h + 2 * e + 1]), c_log2, neg_m));
               l += p0 + p1;
               w[e] = pack_half2(p0, p1);
             }
           } else {
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
-              const int j = 32 * q4 + 2 * e;
+              const int j = 32 * h + 2 * e;
               const float p0 =
-                  j < nvis ? fast_exp2(fmaf(__uint_as_float(v[2 * e]), c_log2, neg_m)) : 0.0f;
+                  j < nvis ? fast_exp2(fmaf(__uint_as_float(v[j]), c_log2, neg_m)) : 0.0f;
               const float p1 =
-                  j + 1 < nvis ? fast_exp2(fmaf(__uint_as_float(v[2 * e + 1]), c_log2, neg_m))
-                               : 0.0f;
+                  j + 1 < nvis ? fast_exp2(fmaf(__uint_as_float(v[j + 1]), c_log2, neg_m)) : 0.0f;
               l += p0 + p1;
               w[e] = pack_half2(p0, p1);
             }
           }
-          tmem_st16(s_tm + 16 * q4, w);
+          tmem_st16(s_tm + 16 * h, w);
         }
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(&pready[X], lane);
+        warp_arrive(&my_pready[gx & 1], lane);
+        if (rr == 0) trace_ev(p, gg, X ? 13 : 4);
       }
       if (fail) break;
       // ---- epilogue: O row / l times the V scale
-      if (!wait_or_abort(&pvdone[X], (gx - 1) & 1, limit, abort_any)) {
-        if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
-        *abort_any = 1;
-        fail = true;
+      if (!wait_or_abort(&my_pvdone[(gx - 1) & 1], ((gx - 1) >> 1) & 1, limit, abort_any)) {
+        note_fail(it);
         break;
       }
       tc_fence_after();
@@ -398,15 +441,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           reinterpret_cast<const __nv_bfloat16*>(p.v_scale) + m.kvh * kHeadDim;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        uint32_t v[16];
-        tmem_ld16(o_tm + 16 * c, v);
+        uint32_t o[16];
+        tmem_ld16(o_tm + 16 * c, o);
         tmem_wait_ld();
         if (row_ok) {
           uint32_t w[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
-            float a0 = __uint_as_float(v[2 * e]) * inv_l;
-            float a1 = __uint_as_float(v[2 * e + 1]) * inv_l;
+            float a0 = __uint_as_float(o[2 * e]) * inv_l;
+            float a1 = __uint_as_float(o[2 * e + 1]) * inv_l;
             if (pc) {
               a0 *= __bfloat162float(vsc[16 * c + 2 * e]);
               a1 *= __bfloat162float(vsc[16 * c + 2 * e + 1]);
@@ -414,14 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               a0 *= vs;
               a1 *= vs;
             }
-            __nv_bfloat162 h = __floats2bfloat162_rn(a0, a1);
-            w[e] = *reinterpret_cast<uint32_t*>(&h);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
+            w[e] = *reinterpret_cast<uint32_t*>(&b2);
           }
           uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
           d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
           d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
         }
       }
+      if (rr == 0) trace_ev(p, gg - 1, X ? 15 : 14);
       if (row_ok) {
         const float ln2 = 0.69314718055994530942f;
         if (m.nch == 1) {
@@ -438,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ CV warpgroup
-    const int t = tid & 127;          // K position / V head dim of the tile
+    const int t = tid & 127;
     uint32_t g = 0;
     bool fail = false;
     auto note_fail = [&](int it) {
@@ -483,69 +527,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = s_base + SM::kRaw + stage * kStageBytes;
         if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
         const int nvalid = min(kTile, m.kv1 - (m.kv0 + i * kTile));
-        // ---- K row of position t -> K16 (rows = positions, two 64-dim halves)
-        if (g > 0 && !wait_or_abort(kfree, (g - 1) & 1, limit, abort_any)) { note_fail(it); break; }
+        // ---- K: thread t converts position t >> 1, dims 64 (t & 1) .. +63,
+        // into K16 buffer g&1 (free once both chains' S of page g-2 completed)
+        if (g >= 2 && !wait_or_abort(&kfree[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
+          note_fail(it);
+          break;
+        }
+        if (t == 0) trace_ev(p, g, 1);
         {
-          const int pg = t >> 6, row = t & 63;
-          const uint32_t src = st + pg * kSlab + row * 128;
+          const int row = t >> 1, half = t & 1;
+          const uint32_t src = st + row * 128;
+          const uint32_t dst = k16 + (g & 1) * kK16Bytes + half * kTile * 128 + row * 128;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c = 4 * half + c4;             // raw chunk: dims 16c .. 16c+15
             uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-            if (t < nvalid) {
+            if (row < nvalid) {
               const uint4 r4 = ld_shared_v4(src + ((c ^ (row & 7)) << 4));
               cvt4<FP8>(r4.x, o0.x, o0.y);
               cvt4<FP8>(r4.y, o0.z, o0.w);
               cvt4<FP8>(r4.z, o1.x, o1.y);
               cvt4<FP8>(r4.w, o1.z, o1.w);
             }
-            // raw chunk c = dims 16c..16c+15 = fp16 chunks 2c, 2c+1 of half c/4
-            const uint32_t dst = k16 + (c >> 2) * kTile * 128 + t * 128;
-            const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
+            const int c0 = 2 * c4, c1 = 2 * c4 + 1;  // fp16 chunks within the half row
+            st_shared_v4(dst + ((c0 ^ (row & 7)) << 4), o0);
+            st_shared_v4(dst + ((c1 ^ (row & 7)) << 4), o1);
+          }
+        }
+        fence_proxy_async_smem();
+        warp_arrive(&kready[g & 1], lane);
+        if (t == 0) trace_ev(p, g, 2);
+        // ---- V^T row of head dim t -> V16 buffer g&1; positions past kv1 are
+        // zero so that P = 0 there meets finite values
+        if (g >= 2 && !wait_or_abort(&vfree[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
+          note_fail(it);
+          break;
+        }
+        if (t == 0) trace_ev(p, g, 5);
+        {
+          const uint32_t src = st + kSlab + t * 64;
+          const uint32_t dst = v16 + (g & 1) * kV16Bytes + t * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int pos = 16 * c;   // first page position of this raw chunk
+            uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+            if (pos < nvalid) {
+              const uint4 r4 = ld_shared_v4(src + ((c ^ ((t >> 1) & 3)) << 4));
+              cvt4<FP8>(r4.x, o0.x, o0.y);
+              cvt4<FP8>(r4.y, o0.z, o0.w);
+              cvt4<FP8>(r4.z, o1.x, o1.y);
+              cvt4<FP8>(r4.w, o1.z, o1.w);
+              if (pos + 16 > nvalid) {
+                uint32_t ww[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                  const int q = pos + 2 * k;
+                  if (q >= nvalid) ww[k] = 0u;
+                  else if (q + 1 >= nvalid) ww[k] &= 0x0000FFFFu;
+                }
+                o0 = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+                o1 = make_uint4(ww[4], ww[5], ww[6], ww[7]);
+              }
+            }
+            const int c0 = 2 * c, c1 = 2 * c + 1;
             st_shared_v4(dst + ((c0 ^ (t & 7)) << 4), o0);
             st_shared_v4(dst + ((c1 ^ (t & 7)) << 4), o1);
           }
         }
         fence_proxy_async_smem();
-        warp_arrive(kready, lane);
-        // ---- V^T row of head dim t -> V16 (rows = dims, one half per page);
-        // positions past kv1 are zero so that P = 0 there meets finite values
-        if (g > 0 && !wait_or_abort(vfree, (g - 1) & 1, limit, abort_any)) { note_fail(it); break; }
-        {
-#pragma unroll
-          for (int pg = 0; pg < 2; ++pg) {
-            const uint32_t src = st + 2 * kSlab + pg * kSlab + t * 64;
-            const uint32_t dst = v16 + pg * kTile * 128 + t * 128;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int pos = pg * 64 + 16 * c;   // first tile position of this raw chunk
-              uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-              if (pos < nvalid) {
-                const uint4 r4 = ld_shared_v4(src + ((c ^ ((t >> 1) & 3)) << 4));
-                cvt4<FP8>(r4.x, o0.x, o0.y);
-                cvt4<FP8>(r4.y, o0.z, o0.w);
-                cvt4<FP8>(r4.z, o1.x, o1.y);
-                cvt4<FP8>(r4.w, o1.z, o1.w);
-                if (pos + 16 > nvalid) {
-                  uint32_t ww[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-#pragma unroll
-                  for (int k = 0; k < 8; ++k) {
-                    const int q = pos + 2 * k;
-                    if (q >= nvalid) ww[k] = 0u;
-                    else if (q + 1 >= nvalid) ww[k] &= 0x0000FFFFu;
-                  }
-                  o0 = make_uint4(ww[0], ww[1], ww[2], ww[3]);
-                  o1 = make_uint4(ww[4], ww[5], ww[6], ww[7]);
-                }
-              }
-              const int c0 = (2 * c) & 7, c1 = (2 * c + 1) & 7;
-              st_shared_v4(dst + ((c0 ^ (t & 7)) << 4), o0);
-              st_shared_v4(dst + ((c1 ^ (t & 7)) << 4), o1);
-            }
-          }
-        }
-        fence_proxy_async_smem();
-        warp_arrive(vready, lane);
+        warp_arrive(&vready[g & 1], lane);
         warp_arrive(&empty[stage], lane);
+        if (t == 0) trace_ev(p, g, 7);
       }
     }
   }

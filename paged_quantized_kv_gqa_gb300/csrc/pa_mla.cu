@@ -227,6 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           for (int bx = 0; bx < nbox; ++bx)
             tma_load_2d(raw + stage * stage_bytes + bx * kBox, &tm_c, &full[stage], 128 * bx, y);
+          trace_ev(p, g, 0);
         }
       }
       for (int s = 0; s < stages; ++s)
@@ -250,6 +251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t d = tmem + kS0 + (g & 1) * kTile;
+          trace_ev(p, g, 5);
           for (int grp = 0; grp < kGroups && ok; ++grp) {
             if (!wait_or_abort(&kready[grp], g & 1, limit, abort_any)) { ok = false; break; }
             tc_fence_after();
@@ -266,6 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           tc_commit(&sfull[g & 1]);
           ++n_s;
+          trace_ev(p, g, 6);
           if (i + 1 == m.ntiles) tc_commit(qfree);
         }
       }
@@ -301,6 +304,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           tc_commit(&pvdone[g & 1]);
+          trace_ev(p, g, 11);
         }
       }
       if (!ok) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
@@ -341,6 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fail = true;
           break;
         }
+        if (t == 0) trace_ev(p, g, 1);
         if (rank == 0) {
           for (int grp = 0; grp < kGroups; ++grp) {
             if (g > 0 && !wait_or_abort(&kfree[grp], (g - 1) & 1, limit, abort_any)) {
@@ -366,6 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (fail) break;
         warp_arrive(&empty[stage], lane);
+        if (t == 0) trace_ev(p, g, 2);
       }
     }
     if (fail) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
@@ -374,6 +380,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // thread = head row (TMEM lane); 576 bf16 -> 288 fp16x2 columns
     const int h = tid & 127;
     bool fail = false;
+    uint32_t g0 = 0;   // first tile of the item (trace only)
     for (int it = item_begin; it < item_end && !fail; ++it) {
       const Item m = load_item<kTile>(p.items, it);
       const int li = it - item_begin;
@@ -382,6 +389,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fail = true;
         break;
       }
+      if (h == 0) trace_ev(p, g0, 3);
       const uint4* src =
           reinterpret_cast<const uint4*>(p.q + (int64_t)m.tok0 * p.q_stride + (int64_t)h * kDqk);
 #pragma unroll 1
@@ -405,6 +413,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_wait_st();
       tc_fence_before();
       warp_arrive(qready, lane);
+      if (h == 0) trace_ev(p, g0, 4);
+      g0 += m.ntiles;
     }
   } else if (rank == 0 && wg == 0) {
     // ================================================================ softmax (score CTA)
@@ -426,6 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t v[64];
         if (ok) {
           tc_fence_after();
+          if (h == 0) trace_ev(p, g, 7);
 #pragma unroll
           for (int c = 0; c < 4; ++c)
             tmem_ld16(t_lane + kS0 + (g & 1) * kTile + 16 * c,
@@ -502,8 +513,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         bar_sync(1, 128);
         if (*abort_sm) { fail = true; break; }
-        if (h == 0)
+        if (h == 0) {
           bulk_s2peer(pin_peer + (g & 1) * kPBuf, buf, kPXfer, (g & 1) ? pfull_peer1 : pfull_peer0);
+          trace_ev(p, g, 8);
+        }
       }
     }
     if (fail) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
@@ -517,6 +530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Item m = load_item<kTile>(p.items, it);
       for (int i = 0; i < m.ntiles; ++i, ++g) {
         if (!wait_or_abort(&pfull[g & 1], (g >> 1) & 1, limit, abort_any)) { fail = true; break; }
+        if (h == 0) trace_ev(p, g, 9);
         const float* meta =
             reinterpret_cast<const float*>(smem + SM::kPin + (g & 1) * kPBuf + kPBytes);
         const float alpha = meta[h];
@@ -543,6 +557,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         warp_arrive(&corr[g & 1], lane);
+        if (h == 0) trace_ev(p, g, 10);
         if (last) {
           if (!wait_or_abort(&pvdone[g & 1], (g >> 1) & 1, limit, abort_any)) { fail = true; break; }
           tc_fence_after();
@@ -571,6 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
           }
           tc_fence_before();
+          if (h == 0) trace_ev(p, g, 12);
         }
       }
     }
