@@ -215,8 +215,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kWarpMmaS) {
     // ================================================================ S issue
     // S_X = Q'_X K16^T for both query tiles, into S buffer (chain tile) & 1;
-    // runs up to two pages ahead of the PV issue
-    if (lane == 0) {
+    // runs up to two pages ahead of the PV issue.  The whole warp runs the
+    // loop (warp-uniform operands); one elected lane issues.
+    {
       const uint32_t idesc_s = idesc_f16_f32(128, kTile);
       uint32_t g = 0, gx[2] = {0, 0};
       bool ok = true;
@@ -239,31 +240,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t s_tm = tmem + X * 128 + (gs & 1) * kTile;
             const uint32_t qa = q_s + X * 128 * 128;
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(s_tm, kstep_desc(qa, kk, kRows * 128), kstep_desc(kb, kk, kTile * 128),
-                     idesc_s, kk > 0 ? 1u : 0u);
-            tc_commit(&sfull[2 * X + (gs & 1)]);
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(s_tm, kstep_desc(qa, kk, kRows * 128), kstep_desc(kb, kk, kTile * 128),
+                       idesc_s, kk > 0 ? 1u : 0u);
+              tc_commit(&sfull[2 * X + (gs & 1)]);
+            }
+            __syncwarp();
             gx[X] = gs + 1;
           }
           if (!ok) break;
-          tc_commit(&kfree[g & 1]);
-          if (i + 1 == m.ntiles) tc_commit(qfree);
-          trace_ev(p, g, 8);
+          if (elect_one()) {
+            tc_commit(&kfree[g & 1]);
+            if (i + 1 == m.ntiles) tc_commit(qfree);
+          }
+          __syncwarp();
+          if (lane == 0) trace_ev(p, g, 8);
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
         *abort_any = 1;
       }
-      // drain: every MMA this thread issued completes before TMEM is released
-      tc_commit(&drain[0]);
+      // drain: every MMA this warp issued completes before TMEM is released
+      if (elect_one()) tc_commit(&drain[0]);
+      __syncwarp();
       mbar_wait(&drain[0], 0, limit);
     }
   } else if (warp == kWarpMmaPV) {
     // ================================================================ PV issue
     // O_X += P_X V16 for both query tiles, P_X read from TMEM (A operand)
-    if (lane == 0) {
+    {
       const uint32_t idesc_pv = idesc_f16_f32(128, kHeadDim);
       uint32_t g = 0, gx[2] = {0, 0};
       bool ok = true;
@@ -282,23 +290,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint32_t p_tm = tmem + X * 128 + (gp & 1) * kTile;
             const uint32_t o_tm = tmem + 256 + X * 128;
+            if (elect_one()) {
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(o_tm, p_tm + 8 * kk, sdesc_k128(vb + kk * 32), idesc_pv,
-                     (i > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&pvdone[2 * X + (gp & 1)]);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(o_tm, p_tm + 8 * kk, sdesc_k128(vb + kk * 32), idesc_pv,
+                       (i > 0 || kk > 0) ? 1u : 0u);
+              tc_commit(&pvdone[2 * X + (gp & 1)]);
+            }
+            __syncwarp();
             gx[X] = gp + 1;
           }
           if (!ok) break;
-          tc_commit(&vfree[g & 1]);
-          trace_ev(p, g, 9);
+          if (elect_one()) tc_commit(&vfree[g & 1]);
+          __syncwarp();
+          if (lane == 0) trace_ev(p, g, 9);
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
         *abort_any = 1;
       }
-      tc_commit(&drain[1]);
+      if (elect_one()) tc_commit(&drain[1]);
+      __syncwarp();
       mbar_wait(&drain[1], 0, limit);
     }
   } else if (wg == 3) {

@@ -228,7 +228,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issue
-    if (lane == 0) {
+    // the whole warp runs the polling loop (warp-uniform operands); one
+    // elected lane issues the MMAs and commits
+    {
       const uint32_t idesc = idesc_f16_f32(128, NR);
       TileCursor cs, cp;       // next S to issue, next PV to issue
       cs.init(p.items, item_begin, item_end);
@@ -245,13 +247,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kb = TM::K0 + (gs & 1) * 64;
           const uint32_t sd = TM::S0 + (gs & 1) * NR;
           const uint32_t qb = q_s + ((cs.it - item_begin) & 1) * NR * 256;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tmem + sd, tmem + kb + 8 * kk,
-                   sdesc_k128(qb + (kk >> 2) * NR * 128 + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
-          tc_commit(&sfull[gs & 1]);
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + sd, tmem + kb + 8 * kk,
+                     sdesc_k128(qb + (kk >> 2) * NR * 128 + (kk & 3) * 32), idesc, kk > 0 ? 1u : 0u);
+            tc_commit(&sfull[gs & 1]);
+          }
+          __syncwarp();
           ++s_commits[gs & 1];
-          trace_ev(p, gs, 8);
+          if (lane == 0) trace_ev(p, gs, 8);
           ++gs;
           cs.advance();
           progressed = true;
@@ -262,14 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vb = TM::V0 + (gp & 1) * 64;
           const uint32_t pb = p_s + (gp & 3) * NR * 256;
           const uint32_t od = TM::O0 + ((cp.it - item_begin) & 1) * NR;
+          if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t bd = sdesc_k128(pb + (kk >> 2) * NR * 128 + (kk & 3) * 32);
-            mma_ts(tmem + od, tmem + vb + 8 * kk, bd, idesc, (cp.i > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t bd = sdesc_k128(pb + (kk >> 2) * NR * 128 + (kk & 3) * 32);
+              mma_ts(tmem + od, tmem + vb + 8 * kk, bd, idesc, (cp.i > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(&pvdone[gp & 3]);
           }
-          tc_commit(&pvdone[gp & 3]);
+          __syncwarp();
           ++pv_commits[gp & 3];
-          trace_ev(p, gp, 9);
+          if (lane == 0) trace_ev(p, gp, 9);
           ++gp;
           cp.advance();
           progressed = true;
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           else if (now - t_idle > limit) { ok = false; break; }
         }
       }
-      if (!ok) {
+      if (!ok && lane == 0) {
         if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
         *abort_any = 1;
       }

@@ -236,7 +236,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (rank == 0 && warp == kWarpMma) {
     // ================================================================ S = Q' K^T (score CTA)
-    if (lane == 0) {
+    // the whole warp runs the loop (warp-uniform operands); one elected lane issues
+    {
       const uint32_t idesc = idesc_f16_f32(128, kTile);
       const uint32_t k16 = s_base + SM::kK16;
       uint32_t g = 0, n_s = 0;
@@ -251,35 +252,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             break;
           }
           const uint32_t d = tmem + kS0 + (g & 1) * kTile;
-          trace_ev(p, g, 5);
+          if (lane == 0) trace_ev(p, g, 5);
           for (int grp = 0; grp < kGroups && ok; ++grp) {
             if (!wait_or_abort(&kready[grp], g & 1, limit, abort_any)) { ok = false; break; }
             tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-            for (int b = 0; b < 3; ++b) {
-              const int kb = 3 * grp + b;
+              for (int b = 0; b < 3; ++b) {
+                const int kb = 3 * grp + b;
 #pragma unroll
-              for (int kq = 0; kq < 4; ++kq)
-                mma_ts(d, tmem + 8 * (4 * kb + kq), sdesc_k128(k16 + kb * kBlk + kq * 32), idesc,
-                       (kb | kq) ? 1u : 0u);
+                for (int kq = 0; kq < 4; ++kq)
+                  mma_ts(d, tmem + 8 * (4 * kb + kq), sdesc_k128(k16 + kb * kBlk + kq * 32), idesc,
+                         (kb | kq) ? 1u : 0u);
+              }
+              tc_commit(&kfree[grp]);
             }
-            tc_commit(&kfree[grp]);
+            __syncwarp();
           }
           if (!ok) break;
-          tc_commit(&sfull[g & 1]);
+          if (elect_one()) {
+            tc_commit(&sfull[g & 1]);
+            if (i + 1 == m.ntiles) tc_commit(qfree);
+          }
+          __syncwarp();
           ++n_s;
-          trace_ev(p, g, 6);
-          if (i + 1 == m.ntiles) tc_commit(qfree);
+          if (lane == 0) trace_ev(p, g, 6);
         }
       }
-      if (!ok) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
+      if (!ok && lane == 0) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
       (void)n_s;
-      tc_commit(drain);   // every MMA this thread issued completes before TMEM is released
+      if (elect_one()) tc_commit(drain);   // every MMA issued completes before TMEM is released
+      __syncwarp();
       mbar_wait(drain, 0, limit);
     }
   } else if (rank == 1 && warp == kWarpMma) {
     // ================================================================ O += P V (value CTA)
-    if (lane == 0) {
+    {
       const uint32_t idesc = idesc_f16_f32_bmn(128, 256);
       const uint32_t v16 = s_base + SM::kV16;
       const uint32_t pin = s_base + SM::kPin;
@@ -289,26 +297,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const Item m = load_item<kTile>(p.items, it);
         for (int i = 0; i < m.ntiles; ++i, ++g) {
           if (!wait_or_abort(&pfull[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
-          mbar_arrive_expect_tx(&pfull[g & 1], kPXfer);   // the P tile two steps ahead
+          if (lane == 0) mbar_arrive_expect_tx(&pfull[g & 1], kPXfer);   // P tile two steps ahead
           if (!wait_or_abort(&corr[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
           const uint32_t pa_ = pin + (g & 1) * kPBuf;
           for (int hv = 0; hv < 2 && ok; ++hv) {
             if (!wait_or_abort(&vready[hv], g & 1, limit, abort_any)) { ok = false; break; }
             tc_fence_after();
+            if (elect_one()) {
 #pragma unroll
-            for (int kq = 0; kq < 4; ++kq)
-              mma_ss(tmem + 256 * hv, sdesc_k128(pa_ + kq * 32),
-                     sdesc_mn128(v16 + 4 * hv * kBlk + kq * 16 * 128, kBlk, 1024), idesc,
-                     (i > 0 || kq > 0) ? 1u : 0u);
-            tc_commit(&vfree[hv]);
+              for (int kq = 0; kq < 4; ++kq)
+                mma_ss(tmem + 256 * hv, sdesc_k128(pa_ + kq * 32),
+                       sdesc_mn128(v16 + 4 * hv * kBlk + kq * 16 * 128, kBlk, 1024), idesc,
+                       (i > 0 || kq > 0) ? 1u : 0u);
+              tc_commit(&vfree[hv]);
+            }
+            __syncwarp();
           }
           if (!ok) break;
-          tc_commit(&pvdone[g & 1]);
-          trace_ev(p, g, 11);
+          if (elect_one()) tc_commit(&pvdone[g & 1]);
+          __syncwarp();
+          if (lane == 0) trace_ev(p, g, 11);
         }
       }
-      if (!ok) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
-      tc_commit(drain);
+      if (!ok && lane == 0) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
+      if (elect_one()) tc_commit(drain);
+      __syncwarp();
       mbar_wait(drain, 0, limit);
     }
   } else if (rank == 1 && warp == kWarpRelay) {
