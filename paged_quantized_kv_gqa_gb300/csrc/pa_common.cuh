@@ -18,13 +18,18 @@ __device__ __forceinline__ void record_status(int32_t* status, int code, int det
 }
 
 // Waits on an mbarrier phase; gives up at the deadline or once any role of the
-// CTA has raised the abort flag.
+// CTA has raised the abort flag.  hint_ns > 0 bounds each suspension of the
+// probe, so a waiting role notices a completed phase within about that time
+// (at the price of more frequent re-probing); 0 leaves it to the hardware.
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int* abort_any) {
-  if (mbar_try_wait(bar, parity)) return true;
+                                              volatile int* abort_any, uint32_t hint_ns = 0) {
+  auto probe = [&]() {
+    return hint_ns ? mbar_try_wait_hint(bar, parity, hint_ns) : mbar_try_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (probe()) return true;
     if (*abort_any) return false;
     if (globaltimer() - t0 > limit_ns) return false;
   }

@@ -56,6 +56,12 @@ constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBufs = 4;                        // P^T ring depth
 
+// The decode pipeline is latency-bound: its waits re-probe every 32 ns.
+__device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                      volatile int* abort_any) {
+  return wait_or_abort(bar, parity, limit_ns, abort_any, 32);
+}
+
 constexpr int stages_for(int nr) { return nr <= 48 ? 4 : 3; }
 
 // TMEM columns: K[2] 0/64, V[2] 128/192, S[2] 256/256+NR, O[2] 256+2NR/256+3NR.
@@ -196,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           int pages[2];
           pages[0] = bt[pos0 / kPage];
           pages[1] = npg == 2 ? bt[pos0 / kPage + 1] : 0;
-          if (!wait_or_abort(&empty[stage], ph ^ 1, limit, abort_any)) {
+          if (!dwait(&empty[stage], ph ^ 1, limit, abort_any)) {
             if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, it);
             *abort_any = 1;
             ok = false;
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto epilogue = [&](int li, uint32_t gl) -> bool {
       const int it = item_begin + li;
       const Item m = load_item<kTileTok>(p.items, it);
-      if (!wait_or_abort(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
+      if (!dwait(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
         note_fail(it);
         return false;
       }
@@ -377,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < cur.ntiles; ++i, ++g) {
         // ---- S_g columns of this half -> registers, then release the S buffer
         float s[NH];
-        if (!fail && !wait_or_abort(&sfull[g & 1], (g >> 1) & 1, limit, abort_any)) note_fail(it);
+        if (!fail && !dwait(&sfull[g & 1], (g >> 1) & 1, limit, abort_any)) note_fail(it);
         tc_fence_after();
         if (tid == 0) trace_ev(p, g, 3);
         if (!fail) {
@@ -446,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < NH; ++j) l[j] *= alpha_s[r_lo + j];
           if (i > 0) {
             // O holds PV of the earlier tiles of this item: wait for the last one
-            if (!fail && !wait_or_abort(&pvdone[(g - 1) & 3], ((g - 1) >> 2) & 1, limit, abort_any))
+            if (!fail && !dwait(&pvdone[(g - 1) & 3], ((g - 1) >> 2) & 1, limit, abort_any))
               note_fail(it);
             tc_fence_after();
             if (!fail) {
@@ -467,7 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // P^T slot g&3 was last read by PV_{g-4}
         if (g >= kPBufs && !fail &&
-            !wait_or_abort(&pvdone[g & 3], ((g - kPBufs) >> 2) & 1, limit, abort_any))
+            !dwait(&pvdone[g & 3], ((g - kPBufs) >> 2) & 1, limit, abort_any))
           note_fail(it);
         if (tid == 0) trace_ev(p, g, 11);
         {
@@ -595,12 +601,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int stage = g % kStages;
         // K buffer g&1 was last read by S_{g-2}; Q' buffer li&1 by the S of item
         // li-2, whose last tile is at most g-2
-        if (g >= 2 && !wait_or_abort(&sfull[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
+        if (g >= 2 && !dwait(&sfull[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
           note_fail(it);
           break;
         }
         if (i == 0) load_q(m, q_s + (li & 1) * NR * 256);
-        if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
+        if (!dwait(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
         if (d == 0) trace_ev(p, g, 1);
         {
           const int box = d >> 6, row = d & 63;
@@ -628,7 +634,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_arrive(&kready[g & 1], lane);
         if (d == 0) trace_ev(p, g, 2);
         // V buffer g&1 was last read by PV_{g-2}
-        if (g >= 2 && !wait_or_abort(&pvdone[(g - 2) & 3], ((g - 2) >> 2) & 1, limit, abort_any)) {
+        if (g >= 2 && !dwait(&pvdone[(g - 2) & 3], ((g - 2) >> 2) & 1, limit, abort_any)) {
           note_fail(it);
           break;
         }
