@@ -24,9 +24,10 @@
 //         maximum, and writes the output.
 //     The S and PV work per page (1152 vs 1024 flop per pair) is nearly
 //     balanced and nothing is computed twice.
-//   * Within each CTA: one TMA warp, one MMA-issue warp, a converter
-//     warpgroup, and the softmax (rank 0) or correction / epilogue (rank 1)
-//     warpgroup; rank 0 also has a warpgroup that loads Q' into TMEM.
+//   * Within each CTA: one TMA warp, one MMA-issue warp, two converter
+//     warpgroups (each converts part of every page; in the score CTA one of
+//     them also loads each item's Q' into TMEM), and the softmax (rank 0) or
+//     correction / epilogue (rank 1) warpgroup.
 //   * The global scale folds into the softmax scale (K) and the epilogue (V).
 #include <cfloat>
 
@@ -47,7 +48,7 @@ constexpr int kVBoxes = 4;
 constexpr int kBlk = 64 * 128;                   // fp16 block: 64 rows x 64 dims
 constexpr int kKBlocks = 9;
 constexpr int kVBlocks = 8;
-constexpr int kGroups = 3;                       // K blocks are handed over in 3 groups of 3
+constexpr int kKSplit = 5;                       // K blocks 0-4 / 5-8 come from two converters
 constexpr int kPBytes = kRows * 128;             // P tile: 128 rows x 64 fp16
 constexpr int kMetaBytes = 1040;                 // alpha[128], inv_l[128], flag, last
 constexpr int kPXfer = kPBytes + kMetaBytes;     // bytes shipped per tile
@@ -154,7 +155,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < 3; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 4);
+      mbar_init(&empty[s], 8);
       mbar_init(&kready[s], 4);
       mbar_init(&kfree[s], 1);
     }
@@ -253,13 +254,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t d = tmem + kS0 + (g & 1) * kTile;
           if (lane == 0) trace_ev(p, g, 5);
-          for (int grp = 0; grp < kGroups && ok; ++grp) {
+          for (int grp = 0; grp < 2 && ok; ++grp) {
             if (!wait_or_abort(&kready[grp], g & 1, limit, abort_any)) { ok = false; break; }
             tc_fence_after();
             if (elect_one()) {
-#pragma unroll
-              for (int b = 0; b < 3; ++b) {
-                const int kb = 3 * grp + b;
+              const int kb0 = grp ? kKSplit : 0, kb1 = grp ? kKBlocks : kKSplit;
+              for (int kb = kb0; kb < kb1; ++kb) {
 #pragma unroll
                 for (int kq = 0; kq < 4; ++kq)
                   mma_ts(d, tmem + 8 * (4 * kb + kq), sdesc_k128(k16 + kb * kBlk + kq * 32), idesc,
@@ -340,16 +340,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
     }
-  } else if (wg == 2) {
-    // ================================================================ converter (both CTAs)
+  } else if (wg == 1 || wg == 2) {
+    // ================================================================ converters (both CTAs)
+    // two warpgroups split each page: score CTA blocks 0-4 / 5-8 (K, 576
+    // dims), value CTA blocks 0-3 / 4-7 (V, 512 dims); in the score CTA the
+    // second one also loads each item's Q' into TMEM
     const int t = tid & 127;
+    const int part = wg == 2 ? 0 : 1;
+    const int blk0 = rank == 0 ? (part ? 5 : 0) : (part ? 4 : 0);
+    const int nblk = rank == 0 ? (part ? 4 : 5) : 4;
+    uint64_t* rdy = rank == 0 ? &kready[part] : &vready[part];
+    uint64_t* fre = rank == 0 ? &kfree[part] : &vfree[part];
     const uint32_t raw0 = s_base + (rank == 0 ? SM::kRaw0 : SM::kRaw1);
     const uint32_t stage_bytes = (uint32_t)((rank == 0 ? kKBoxes : kVBoxes) * kBox);
     const uint32_t dst = s_base + (rank == 0 ? SM::kK16 : SM::kV16);
+    const bool q_loader = rank == 0 && part == 1;
     uint32_t g = 0;
     bool fail = false;
     for (int it = item_begin; it < item_end && !fail; ++it) {
       const Item m = load_item<kTile>(p.items, it);
+      const int li = it - item_begin;
+      if (q_loader) {
+        // Q' of the item -> TMEM (thread = head row; 576 bf16 -> 288 fp16x2
+        // columns) once the S MMAs of the previous item completed
+        if (li > 0 && !wait_or_abort(qfree, (li - 1) & 1, limit, abort_any)) {
+          fail = true;
+          break;
+        }
+        if (t == 0) trace_ev(p, g, 3);
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (int64_t)m.tok0 * p.q_stride +
+                                                          (int64_t)t * kDqk);
+#pragma unroll 1
+        for (int c0 = 0; c0 < 18; c0 += 2) {
+          uint4 r[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) r[k] = src[4 * c0 + k];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&r[4 * c + k]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                w[4 * k + e] =
+                    pack_half2(__bfloat162float(hv[2 * e]), __bfloat162float(hv[2 * e + 1]));
+            }
+            tmem_st16(t_lane + 16 * (c0 + c), w);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        warp_arrive(qready, lane);
+        if (t == 0) trace_ev(p, g, 4);
+      }
       for (int i = 0; i < m.ntiles; ++i, ++g) {
         const int stage = (int)(g % (uint32_t)stages);
         const uint32_t raw = raw0 + stage * stage_bytes;
@@ -358,77 +402,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           fail = true;
           break;
         }
-        if (t == 0) trace_ev(p, g, 1);
-        if (rank == 0) {
-          for (int grp = 0; grp < kGroups; ++grp) {
-            if (g > 0 && !wait_or_abort(&kfree[grp], (g - 1) & 1, limit, abort_any)) {
-              fail = true;
-              break;
-            }
-#pragma unroll
-            for (int b = 0; b < 3; ++b) convert_block<FP8>(raw, dst, 3 * grp + b, t, nvalid);
-            fence_proxy_async_smem();
-            warp_arrive(&kready[grp], lane);
-          }
-        } else {
-          for (int hv = 0; hv < 2; ++hv) {
-            if (g > 0 && !wait_or_abort(&vfree[hv], (g - 1) & 1, limit, abort_any)) {
-              fail = true;
-              break;
-            }
-#pragma unroll
-            for (int b = 0; b < 4; ++b) convert_block<FP8>(raw, dst, 4 * hv + b, t, nvalid);
-            fence_proxy_async_smem();
-            warp_arrive(&vready[hv], lane);
-          }
+        if (t == 0 && part == 0) trace_ev(p, g, 1);
+        // this part's fp16 blocks were last read by the MMAs of page g-1
+        if (g > 0 && !wait_or_abort(fre, (g - 1) & 1, limit, abort_any)) {
+          fail = true;
+          break;
         }
-        if (fail) break;
+        for (int b = 0; b < nblk; ++b) convert_block<FP8>(raw, dst, blk0 + b, t, nvalid);
+        fence_proxy_async_smem();
+        warp_arrive(rdy, lane);
         warp_arrive(&empty[stage], lane);
-        if (t == 0) trace_ev(p, g, 2);
+        if (t == 0 && part == 0) trace_ev(p, g, 2);
       }
     }
-    if (fail) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
-  } else if (rank == 0 && wg == 1) {
-    // ================================================================ Q' -> TMEM (score CTA)
-    // thread = head row (TMEM lane); 576 bf16 -> 288 fp16x2 columns
-    const int h = tid & 127;
-    bool fail = false;
-    uint32_t g0 = 0;   // first tile of the item (trace only)
-    for (int it = item_begin; it < item_end && !fail; ++it) {
-      const Item m = load_item<kTile>(p.items, it);
-      const int li = it - item_begin;
-      if (li > 0 && !wait_or_abort(qfree, (li - 1) & 1, limit, abort_any)) {
-        raise_abort(PA_ERR_DEVICE_TIMEOUT, it);
-        fail = true;
-        break;
-      }
-      if (h == 0) trace_ev(p, g0, 3);
-      const uint4* src =
-          reinterpret_cast<const uint4*>(p.q + (int64_t)m.tok0 * p.q_stride + (int64_t)h * kDqk);
-#pragma unroll 1
-      for (int c0 = 0; c0 < 18; c0 += 3) {
-        uint4 r[12];
-#pragma unroll
-        for (int k = 0; k < 12; ++k) r[k] = src[4 * c0 + k];
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          uint32_t w[16];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&r[4 * c + k]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w[4 * k + e] = pack_half2(__bfloat162float(hv[2 * e]), __bfloat162float(hv[2 * e + 1]));
-          }
-          tmem_st16(t_lane + 16 * (c0 + c), w);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      warp_arrive(qready, lane);
-      if (h == 0) trace_ev(p, g0, 4);
-      g0 += m.ntiles;
-    }
+    if (fail && t == 0) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
   } else if (rank == 0 && wg == 0) {
     // ================================================================ softmax (score CTA)
     const int h = tid & 127;
