@@ -31,7 +31,7 @@ from typing import Optional
 import numpy as np
 
 from . import rng
-from .formats import to_bf16_bits, to_e4m3_bytes, int8_to_bytes, E4M3_MAX
+from .formats import to_bf16_bits, bf16_bits_to_f64, to_e4m3_bytes, int8_to_bytes, E4M3_MAX
 
 # counter streams
 S_LEN_KV = 1
@@ -42,6 +42,8 @@ S_V = 5
 S_KSCALE = 6
 S_VSCALE = 7
 S_PERM = 8
+S_KNEW = 9
+S_VNEW = 10
 
 INT8 = "int8"
 FP8 = "fp8_e4m3"
@@ -367,3 +369,39 @@ def config(n: int) -> Case:
                          kv_dtype=FP8, scale_kind=GLOBAL, layout=MLA, causal=True,
                          chunk_size=-1, sm_scale=1.0 / math.sqrt(192.0))
     raise ValueError(n)
+
+
+def new_kv(case: Case):
+    """bf16 keys / values of the appended tokens, to be quantised into the cache.
+
+    GQA: (k [T, kv_heads, Dqk], v [T, kv_heads, Dv]) bf16 bit patterns; MLA:
+    (k [T, Dqk], None).  Values are N(0, 1) times the stored-value spread of
+    the cache: 40 x the channel's scale for int8 (so x / s mostly stays within
+    +-127 and a few values saturate), 1 for fp8 (its scales map the N(0, 1)
+    pool onto +-448).
+    """
+    T = case.total_q
+
+    def draws(stream, shape, spread):
+        n = int(np.prod(shape))
+        x = rng.normal(case.seed, stream, np.arange(n, dtype=np.uint64)).reshape(shape)
+        return to_bf16_bits(x * spread)
+
+    def spread(which, heads, D):
+        if case.kv_dtype == FP8:
+            return 1.0
+        sc = case.k_scale if which == "k" else case.v_scale
+        if case.scale_kind == GLOBAL:
+            return 40.0 * float(np.asarray(sc, np.float32).reshape(-1)[0])
+        s = bf16_bits_to_f64(np.asarray(sc, np.uint16))
+        if case.scale_kind == PER_HEAD:
+            return 40.0 * s.reshape(heads, 1)
+        return 40.0 * s.reshape(heads, D)
+
+    if case.layout == MLA:
+        return draws(S_KNEW, (T, case.head_dim_qk), spread("k", 1, case.head_dim_qk)), None
+    k = draws(S_KNEW, (T, case.kv_heads, case.head_dim_qk),
+              spread("k", case.kv_heads, case.head_dim_qk))
+    v = draws(S_VNEW, (T, case.kv_heads, case.head_dim_v),
+              spread("v", case.kv_heads, case.head_dim_v))
+    return k, v
