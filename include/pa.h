@@ -200,6 +200,30 @@ void pa_plan_destroy(pa_plan_t* plan);
 const char* pa_last_error(void);
 
 /*
+ * pa_cache_append: quantises the appended tokens' keys and values and writes
+ * them into the paged cache, at positions seq_lens_kv[b] .. seq_lens_kv[b] +
+ * seq_lens[b] - 1 of each sequence (the step before pa_run; the pages'
+ * attention kernels read the cache in exactly this layout and convention:
+ * FastDeploy append_attention_c8_impl.cuh K [page][kv head][B][D], V
+ * transposed per page [page][kv head][D][B], real = stored x scale; XQA
+ * mla_sm120.cu one latent row per position with one global scale).
+ *   stored byte = Q(x / s): the IEEE binary32 quotient of the bf16 input x and
+ *   its scale s (per kv head, per channel kv_head * D + d, or the global fp32
+ *   scale), then int8 round-half-even saturated to +-127, or E4M3
+ *   round-to-nearest-even saturated to +-448.
+ *   k_new, v_new: device bf16, token t's row at t * kv_stride elements, kv head
+ *   h at h * D within it (MLA: the 576-wide latent row; v_new unused, may be
+ *   NULL).  A packed qkv tensor works with kv_stride = (Hq + 2 Hkv) * D.
+ *   args: cache_k / cache_v (written), k_scale / v_scale, block_table and the
+ *   device seq_lens, seq_lens_kv, cu_seqlens_q; q, out, lse unused.
+ *   workspace: as for pa_run (its status word records PA_ERR_BAD_PAGE for a
+ *   block_table entry outside the pool; read it with pa_check).
+ * Asynchronous on stream; no allocation.
+ */
+pa_status pa_cache_append(const pa_plan_t* plan, const pa_args* args, const void* k_new,
+                          const void* v_new, int64_t kv_stride, void* workspace, void* stream);
+
+/*
  * pa_run_static: plan upload + pa_run + pa_merge in one call, using a
  * workspace that lives inside the library instead of one the caller
  * allocates.  (The source pages have no counterpart; this entry point exists

@@ -79,6 +79,7 @@ def _load():
         "pa_debug_set_faults": ([i64, i32], i32),
         "pa_run_static": ([vp, ctypes.POINTER(PaArgs), vp, i32], i32),
         "pa_debug_set_trace": ([vp, i32, i32], i32),
+        "pa_cache_append": ([vp, ctypes.POINTER(PaArgs), vp, vp, i64, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -238,6 +239,14 @@ def pa_run_static(plan: Plan, args: PaArgs, stream=None, check: bool = False):
     (for callers that cannot allocate device memory; see include/pa.h).
     check=True synchronises the stream and raises on a device-side error."""
     _check(lib.pa_run_static(plan.handle, ctypes.byref(args), _stream(stream), int(bool(check))))
+
+
+def pa_cache_append(plan: Plan, args: PaArgs, k_new, v_new, kv_stride: int, workspace,
+                    stream=None):
+    """Quantise the appended tokens' K / V rows (bf16, token stride kv_stride
+    elements) into the paged cache of args (see include/pa.h)."""
+    _check(lib.pa_cache_append(plan.handle, ctypes.byref(args), _ptr(k_new), _ptr(v_new),
+                               int(kv_stride), _ptr(workspace), _stream(stream)))
 
 
 def pa_debug_set_trace(buf=None, ctas: int = 0, tiles_per_cta: int = 0):

@@ -103,6 +103,7 @@ static pa_status build_plan(const pa_problem& prob, const int32_t* ql, const int
     max_q = std::max(max_q, ql[b]);
   }
   P.total_q = bsz > 0 ? cu[bsz] : 0;
+  P.max_q = max_q;
 
   int rows_cap, per_item;
   if (prob.layout == PA_LAYOUT_MLA) {
@@ -535,6 +536,28 @@ pa_status pa_debug_gather(const pa_problem* problem, const pa_args* args, int32_
   cudaError_t e = launch_gather(*problem, *args, b, kv_head, pos0, n, dst_k, dst_v,
                                 static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("gather: ") + cudaGetErrorString(e));
+  return PA_OK;
+}
+
+pa_status pa_cache_append(const pa_plan_t* plan, const pa_args* args, const void* k_new,
+                          const void* v_new, int64_t kv_stride, void* workspace, void* stream) {
+  if (!plan || !args || !workspace) return fail(PA_ERR_INVALID_ARG, "null plan, args or workspace");
+  const pa_problem& pr = plan->prob;
+  const bool mla = pr.layout == PA_LAYOUT_MLA;
+  if (!args->cache_k || !args->k_scale || !args->block_table || !args->seq_lens ||
+      !args->seq_lens_kv || !args->cu_seqlens_q || !k_new)
+    return fail(PA_ERR_INVALID_ARG, "null device pointer for the cache append");
+  if (!mla && (!args->cache_v || !args->v_scale || !v_new))
+    return fail(PA_ERR_INVALID_ARG, "null V cache, V scale or new V rows");
+  const int64_t row = mla ? pr.head_dim_qk : (int64_t)pr.kv_heads * pr.head_dim_qk;
+  if (kv_stride < row)
+    return fail(PA_ERR_INVALID_ARG, "kv_stride smaller than one token's K / V row");
+  if (reinterpret_cast<uintptr_t>(k_new) % 2 || reinterpret_cast<uintptr_t>(v_new) % 2)
+    return fail(PA_ERR_INVALID_ARG, "new K / V rows must be 2-byte aligned (bf16)");
+  cudaError_t e = launch_cache_append(*plan, *args, k_new, v_new, kv_stride,
+                                      static_cast<int32_t*>(workspace),
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("cache append: ") + cudaGetErrorString(e));
   return PA_OK;
 }
 

@@ -1,0 +1,142 @@
+// pa_cache.cu - quantise-and-write of the appended tokens' K / V into the paged
+// int8 / FP8-E4M3 cache (the step before the attention path).
+//
+// Layouts and value convention are the ones the attention kernels read
+// (FastDeploy append_attention_c8_impl.cuh: K [page][kv head][64][D], V
+// transposed per page [page][kv head][D][64], real = stored x scale; XQA
+// mla_sm120.cu: one latent row [page][64][576] per position, one global
+// scale).  Token i of sequence b goes to position seq_lens_kv[b] + i.  The
+// stored byte is Q(x / s): the IEEE binary32 quotient of the bf16 input and
+// its scale, then int8 round-half-even saturated to +-127, or E4M3
+// round-to-nearest-even saturated to +-448.
+//
+// One CTA per (sequence, page of the appended range, kv head), thread = head
+// dim: reads of the new rows and writes of K rows are coalesced; each thread
+// writes its own V^T row segment.
+#include "pa_common.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int kPage = 64;
+constexpr int kThreads = 128;
+
+template <int FP8>
+__device__ __forceinline__ uint8_t quantize(float x, float s) {
+  const float v = __fdiv_rn(x, s);
+  if constexpr (FP8) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+    return (uint8_t)(r & 0xFF);
+  } else {
+    const int q = max(-127, min(127, __float2int_rn(v)));
+    return (uint8_t)(q & 0xFF);
+  }
+}
+
+struct AppendParams {
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t kv_stride;         // elements between consecutive tokens' rows
+  uint8_t* cache_k;
+  uint8_t* cache_v;
+  const void* k_scale;
+  const void* v_scale;
+  const int32_t* block_table;
+  const int32_t* seq_lens;
+  const int32_t* seq_lens_kv;
+  const int32_t* cu_seqlens_q;
+  int32_t* status;
+  int32_t max_blocks;
+  int32_t num_pages;
+  int32_t kv_heads;
+  int32_t head_dim;          // GQA 128; MLA 576 (row width)
+  int32_t scale_kind;
+  int32_t mla;
+};
+
+template <int FP8>
+__global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendParams p) {
+  const int b = blockIdx.x;
+  const int kvh = blockIdx.z;
+  const int q = p.seq_lens[b];
+  if (q <= 0) return;
+  const int start = p.seq_lens_kv[b];
+  const int end = start + q;
+  const int lp = start / kPage + (int)blockIdx.y;
+  const int p0 = max(lp * kPage, start), p1 = min(lp * kPage + kPage, end);
+  if (p0 >= p1) return;
+  const int page = p.block_table[(int64_t)b * p.max_blocks + lp];
+  if (page < 0 || page >= p.num_pages) {
+    if (threadIdx.x == 0 && atomicCAS(p.status, 0, PA_ERR_BAD_PAGE) == 0) {
+      p.status[1] = b;
+      p.status[2] = (int)blockIdx.x;
+    }
+    return;
+  }
+  const int t0 = p.cu_seqlens_q[b] + (p0 - start);
+  if (p.mla) {
+    // whole latent rows: row pos -> cache[page][pos % 64][0 .. 576)
+    const float s = reinterpret_cast<const float*>(p.k_scale)[0];
+    for (int pos = p0; pos < p1; ++pos) {
+      const __nv_bfloat16* src = p.k_new + (int64_t)(t0 + pos - p0) * p.kv_stride;
+      uint8_t* dst = p.cache_k + ((int64_t)page * kPage + (pos % kPage)) * p.head_dim;
+      for (int d = threadIdx.x; d < p.head_dim; d += kThreads)
+        dst[d] = quantize<FP8>(__bfloat162float(src[d]), s);
+    }
+    return;
+  }
+  const int d = threadIdx.x;   // head dim (GQA head_dim 128)
+  const float sk = load_scale(p.k_scale, p.scale_kind,
+                              p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * 128 + d : kvh);
+  const float sv = load_scale(p.v_scale, p.scale_kind,
+                              p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * 128 + d : kvh);
+  const int64_t slab = (int64_t)page * p.kv_heads + kvh;
+  uint8_t* krow = p.cache_k + slab * kPage * 128;
+  uint8_t* vrow = p.cache_v + (slab * 128 + d) * kPage;
+  for (int pos = p0; pos < p1; ++pos) {
+    const int64_t t = (int64_t)(t0 + pos - p0);
+    const float xk = __bfloat162float(p.k_new[t * p.kv_stride + (int64_t)kvh * 128 + d]);
+    const float xv = __bfloat162float(p.v_new[t * p.kv_stride + (int64_t)kvh * 128 + d]);
+    krow[(pos % kPage) * 128 + d] = quantize<FP8>(xk, sk);
+    vrow[pos % kPage] = quantize<FP8>(xv, sv);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_append(const Plan& plan, const pa_args& a, const void* k_new,
+                                const void* v_new, int64_t kv_stride, int32_t* status,
+                                cudaStream_t stream) {
+  const pa_problem& pr = plan.prob;
+  if (pr.bsz == 0 || plan.max_q == 0) return cudaSuccess;
+  AppendParams p{};
+  p.k_new = static_cast<const __nv_bfloat16*>(k_new);
+  p.v_new = static_cast<const __nv_bfloat16*>(v_new);
+  p.kv_stride = kv_stride;
+  p.cache_k = static_cast<uint8_t*>(const_cast<void*>(a.cache_k));
+  p.cache_v = static_cast<uint8_t*>(const_cast<void*>(a.cache_v));
+  p.k_scale = a.k_scale;
+  p.v_scale = a.v_scale;
+  p.block_table = a.block_table;
+  p.seq_lens = a.seq_lens;
+  p.seq_lens_kv = a.seq_lens_kv;
+  p.cu_seqlens_q = a.cu_seqlens_q;
+  p.status = status;
+  p.max_blocks = pr.max_blocks_per_seq;
+  p.num_pages = pr.num_pages;
+  p.kv_heads = pr.kv_heads;
+  p.head_dim = pr.head_dim_qk;
+  p.scale_kind = pr.scale_kind;
+  p.mla = pr.layout == PA_LAYOUT_MLA ? 1 : 0;
+  // pages an appended range of max_q positions can touch
+  const int npg = (plan.max_q + kPage - 1) / kPage + 1;
+  const dim3 grid(pr.bsz, npg, p.mla ? 1 : pr.kv_heads);
+  if (pr.kv_dtype == PA_KV_FP8_E4M3)
+    cache_append_kernel<1><<<grid, kThreads, 0, stream>>>(p);
+  else
+    cache_append_kernel<0><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -32,6 +32,7 @@ struct Plan {
   int32_t max_chunks = 1;
   int32_t num_sms = 0;
   int32_t decode_rows = 0;    // padded row count (decode family)
+  int32_t max_q = 0;          // longest query run (appended tokens per sequence)
   std::vector<int32_t> items;        // [n][8] CTA-major
   std::vector<int32_t> work_indptr;  // [num_ctas+1]
   std::vector<int32_t> nch_token;    // [T]
@@ -107,6 +108,9 @@ cudaError_t launch_append(const Plan& plan, const AttnParams& p, const CUtensorM
                           const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream);
 cudaError_t launch_mla(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_c,
                        cudaStream_t stream);
+cudaError_t launch_cache_append(const Plan& plan, const pa_args& a, const void* k_new,
+                                const void* v_new, int64_t kv_stride, int32_t* status,
+                                cudaStream_t stream);
 cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
                          cudaStream_t stream);
 cudaError_t launch_gather(const pa_problem& prob, const pa_args& a, int32_t b, int32_t kvh,
