@@ -53,9 +53,9 @@ def _peaks(bound: str):
 # `ncu --set full` capture (summaries under profiles/).  A figure is reported
 # only while the kernel source still hashes to the version it was taken with.
 NCU_TRAFFIC = {
-    "decode-2": ("pa_decode.cu", "3a7c273e7c0864e5", 319.308032e6 + 4.890368e6),
-    "append-3": ("pa_append.cu", "388089fb01ca7b40", 72.266496e6 + 2.511104e6),
-    "mla-5": ("pa_mla.cu", "1b3ae6c0e072d3f4", 199.242752e6 + 23.372288e6),
+    "decode-2": ("pa_decode.cu", "f5eb6755bf6df5db", 319.333632e6 + 5.314560e6),
+    "append-3": ("pa_append.cu", "d3108ca4e473eb65", 72.359168e6 + 3.082240e6),
+    "mla-5": ("pa_mla.cu", "61e949fe9751d07a", 199.316224e6 + 23.848960e6),
 }
 
 
@@ -293,6 +293,117 @@ def run_cuda(args) -> dict:
     return res if rank == 0 else None
 
 
+def run_cache_append(args) -> dict:
+    """Times pa_cache_append: the appended tokens of a workload (default the
+    append workload's 2.3K tokens x 8 kv heads) quantised into the paged cache.
+    Metric: bytes of the bf16 rows read plus cache bytes written, per second."""
+    import torch
+    import paged_quantized_kv_gqa_gb300 as pa
+    from synth.device import to_device
+    from synth.cases import new_kv
+
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    case = _workload(args.config)
+    d = to_device(case, dev)
+    k, v = new_kv(case)
+    kd = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).to(dev)
+    vd = None if v is None else torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).to(dev)
+    stride = kd[0].numel()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    plan = pa.pa_plan(pa.problem_of(case), case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, sms)
+    ws = torch.zeros(plan.workspace_size, dtype=torch.uint8, device=dev)
+    cargs = pa.make_args(q=d["q"], cache_k=d["cache_k"], cache_v=d["cache_v"],
+                         k_scale=d["k_scale"], v_scale=d["v_scale"], block_table=d["block_table"],
+                         out=d["out"], lse=d["lse"], seq_lens=d["seq_lens"],
+                         seq_lens_kv=d["seq_lens_kv"], cu_seqlens_q=d["cu_seqlens_q"])
+    stream = torch.cuda.current_stream(dev)
+    pa.pa_plan_upload(plan, ws, stream)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    vals = kd.numel() + (0 if vd is None else vd.numel())
+    nbytes = vals * 3                      # bf16 read + one stored byte each
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        pa.pa_cache_append(plan, cargs, kd, vd, stride, ws, stream)
+    st, _ = pa.pa_check(plan, ws, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    _barrier(world)
+    torch.cuda.synchronize(dev)
+    with Clocks(local) as clk:
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            pa.pa_cache_append(plan, cargs, kd, vd, stride, ws, stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+    _barrier(world)
+    ms = _max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in ev), world)
+    work = nbytes / 1e9
+    peak, peak_kind = _peaks("hbm")
+    # end to end: the new rows up from pinned host memory, the status word back
+    kh = kd.cpu().pin_memory()
+    vh = None if vd is None else vd.cpu().pin_memory()
+    sth = torch.empty(4, dtype=torch.int32).pin_memory()
+    e2e_ms = []
+    for i in range(max(3, K)):
+        flush.fill_(i & 0xFF)
+        a, b = ev[i % K]
+        a.record(stream)
+        kd.copy_(kh, non_blocking=True)
+        if vd is not None:
+            vd.copy_(vh, non_blocking=True)
+        pa.pa_cache_append(plan, cargs, kd, vd, stride, ws, stream)
+        sth.copy_(ws[:16].view(torch.int32), non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = _job_rate(work, world, _max_over_ranks(statistics.mean(e2e_ms), world))
+    res = {
+        "metric": "KV-cache append (quantise + paged write) GB/s", "value": round(_job_rate(work, world, ms), 2),
+        "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 quotient -> int8 / e4m3 bytes", "data": "synthetic",
+        "config": {"workload": case.name + " appended tokens", "tokens": case.total_q,
+                   "bytes_per_step": nbytes, "l2": "flushed (512 MiB write) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(work / (ms * 1e-3), 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(work / (ms * 1e-3) / peak, 4), "traffic": None,
+                     "peak_source": peak_kind, "kernel": "pa_cache_append kernel", "run_ms": round(ms, 5)},
+        "e2e": {"value": round(e2e, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(vals * 2), "d2h_bytes_per_step": 16},
+        "gpu_launches": K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        from oracle import cache_append as ca
+        t0 = time.perf_counter()
+        n = 0
+        sub = synth_subcase(case, max(1, case.bsz // 8))
+        sk, sv = new_kv(sub)
+        ca.cache_append(sub, sk, sv, sub.cache_k, sub.cache_v if sub.layout != "mla" else None)
+        dt = time.perf_counter() - t0
+        nb = (sk.size + (0 if sv is None else sv.size)) * 3
+        res["cpu_baseline"] = {"value": round(nb / dt / 1e9, 6), "unit": "GB/s", "cores": 1,
+                               "kind": "oracle", "sample": f"{sub.total_q} appended tokens "
+                               f"({sub.bsz} of {case.bsz} sequences), {dt:.1f} s, numpy"}
+    return res if rank == 0 else None
+
+
+def synth_subcase(case, nseq: int):
+    """The first nseq sequences of a workload as a case of its own."""
+    import synth
+    kw = dict(name=case.name + "-sample", seed=case.seed, seq_lens=case.seq_lens[:nseq],
+              seq_lens_kv=case.seq_lens_kv[:nseq], q_heads=case.q_heads, kv_heads=case.kv_heads,
+              head_dim_qk=case.head_dim_qk, head_dim_v=case.head_dim_v, kv_dtype=case.kv_dtype,
+              scale_kind=case.scale_kind, layout=case.layout, causal=case.causal)
+    return synth.make_case(**kw)
+
+
 def synth_desc(n: int) -> str:
     import synth
     return synth.CONFIG_NAMES[n]
@@ -364,10 +475,16 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="attention", choices=["attention", "cache-append"],
+                    help="attention: the path (default); cache-append: the quantise-and-write "
+                         "step before it, on the workload's appended tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    res = run_reference(args) if args.impl == "reference" else run_cuda(args)
+    if args.op == "cache-append" and args.impl != "reference":
+        res = run_cache_append(args)
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_cuda(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 
