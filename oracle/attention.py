@@ -111,12 +111,24 @@ def q_rows(p, b: int, kvh: int) -> np.ndarray:
 
 
 def _visible(p, b: int, q_len: int, kvtot: int, lo: int, hi: int) -> np.ndarray:
-    """Boolean [q_len, kvtot] mask: causal bound, sequence end and chunk [lo, hi)."""
+    """Boolean [q_len, kvtot] mask: causal bound, sequence end and chunk [lo, hi).
+
+    With a speculative tree mask (FastDeploy append_attention_c8_impl.cuh,
+    attn_mask [bsz, max_q, max_q] among the draft tokens), appended position
+    seq_lens_kv + c is visible to appended token i only if attn_mask[b, i, c]
+    is set; the cached prefix stays visible to every token.
+    """
     j = np.arange(kvtot)[None, :]
     i = np.arange(q_len)[:, None]
     vis = (j >= lo) & (j < hi)
+    pre = int(p.seq_lens_kv[b])
     if p.causal:
-        vis = vis & (j <= int(p.seq_lens_kv[b]) + i)
+        vis = vis & (j <= pre + i)
+    mask = getattr(p, "attn_mask", None)
+    if mask is not None:
+        c = np.clip(j - pre, 0, mask.shape[2] - 1)
+        tm = np.asarray(mask[b])[np.arange(q_len)[:, None], c] != 0
+        vis = vis & ((j < pre) | tm)
     return vis
 
 

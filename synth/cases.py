@@ -44,6 +44,7 @@ S_VSCALE = 7
 S_PERM = 8
 S_KNEW = 9
 S_VNEW = 10
+S_TREE = 11
 
 INT8 = "int8"
 FP8 = "fp8_e4m3"
@@ -83,6 +84,9 @@ class Case:
     k_scale: np.ndarray         # uint16 bf16 bits [Hkv] / [Hkv*D], or float32 [1]
     v_scale: np.ndarray
     int8_range: tuple = (-127, 127)
+    # optional speculative tree mask [bsz, max_q, max_q] uint8: appended token i
+    # of a sequence sees appended token j iff attn_mask[b, i, j] (and j <= i)
+    attn_mask: Optional[np.ndarray] = None
     _cache_k: Optional[np.ndarray] = None
     _cache_v: Optional[np.ndarray] = None
     _page_memo: Optional[dict] = None
@@ -405,3 +409,20 @@ def new_kv(case: Case):
     v = draws(S_VNEW, (T, case.kv_heads, case.head_dim_v),
               spread("v", case.kv_heads, case.head_dim_v))
     return k, v
+
+
+def tree_mask(case: Case) -> np.ndarray:
+    """A seeded draft tree per sequence: appended token 0 is the root, token i
+    > 0 hangs under a parent drawn uniformly from 0 .. i-1, and a token sees
+    itself and its ancestors.  Returns uint8 [bsz, max_q, max_q]."""
+    max_q = int(case.seq_lens.max()) if case.bsz else 0
+    m = np.zeros((case.bsz, max_q, max_q), np.uint8)
+    for b in range(case.bsz):
+        n = int(case.seq_lens[b])
+        for i in range(n):
+            if i > 0:
+                parent = int(rng.uniform_int(case.seed, S_TREE,
+                                             np.array([b * 4096 + i], np.uint64), 0, i - 1)[0])
+                m[b, i] = m[b, parent]
+            m[b, i, i] = 1
+    return m

@@ -107,6 +107,9 @@ def brute(case):
                 t = int(case.cu_seqlens_q[b]) + i
                 q = bf(case.q_bits[t, h * D:(h + 1) * D])
                 mask = np.array([(not case.causal) or j <= pre + i for j in range(n)])
+                if case.attn_mask is not None:   # draft tree: ancestors among appended tokens
+                    mask &= np.array([j < pre or bool(case.attn_mask[b, i, j - pre])
+                                      for j in range(n)])
                 s = torch.from_numpy(case.sm_scale * (K @ q))
                 s[~torch.from_numpy(mask)] = -torch.inf
                 w = torch.softmax(s, dim=0).numpy()
@@ -274,3 +277,46 @@ def test_workload_shapes():
     c4 = synth.config(4)
     assert (c4.seq_lens == 6).all() and c4.q_heads == 64 and c4.chunk_size == 1024
     assert c4.seq_lens_kv.min() >= 8192 and c4.seq_lens_kv.max() <= 32768
+
+
+def _with_mask(case, mask):
+    case.attn_mask = mask
+    return case
+
+
+def test_tree_mask_brute_force_agrees():
+    """The draft-tree visibility rule against the element-by-element evaluation."""
+    from synth.cases import tree_mask
+    case = small_case(seq_lens=[6, 1, 5], seq_lens_kv=[70, 0, 129])
+    _with_mask(case, tree_mask(case))
+    assert case.attn_mask[0].sum() > 6 and not np.all(np.tril(case.attn_mask[0]) == 1)
+    out, lse = oa.reference(case)
+    bo, bl = brute(case)
+    assert np.allclose(out, bo, rtol=0, atol=1e-12)
+    assert np.allclose(lse, bl, rtol=0, atol=1e-12)
+
+
+def test_full_lower_triangular_tree_is_causal():
+    """A chain (every token sees all earlier draft tokens) is plain causal."""
+    case = small_case(seq_lens=[6, 3], seq_lens_kv=[40, 64])
+    o1, l1 = oa.reference(case)
+    _with_mask(case, np.tril(np.ones((2, 6, 6), np.uint8)))
+    o2, l2 = oa.reference(case)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_root_only_tree_sees_prefix_and_itself():
+    """With no edges, token i attends over the prefix and its own position only:
+    the same as a single-token decode at position seq_lens_kv + i."""
+    case = small_case(seq_lens=[4], seq_lens_kv=[100])
+    _with_mask(case, np.eye(4, dtype=np.uint8)[None])
+    out, lse = oa.reference(case)
+    S, V, kvtot = oa.unit_scores(case, 0, 0)
+    G = case.q_heads // case.kv_heads
+    for i in range(4):
+        idx = np.r_[np.arange(100), 100 + i]
+        s = S[i, :, idx].T                      # [G, n]
+        m = s.max(axis=1, keepdims=True)
+        w = np.exp(s - m)
+        ref = (w @ V[idx]) / w.sum(axis=1, keepdims=True)
+        assert np.allclose(out[i, :G], ref, rtol=0, atol=1e-12)
