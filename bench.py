@@ -182,6 +182,10 @@ def run_cuda(args) -> dict:
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     case = _workload(args.config)
+    if args.tree_mask:
+        from synth.cases import tree_mask
+        case.attn_mask = tree_mask(case)
+        case.name += " tree-mask"
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     d = to_device(case, dev)
     plan = pa.pa_plan(pa.problem_of(case), case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, sms)
@@ -189,7 +193,9 @@ def run_cuda(args) -> dict:
     ws = torch.zeros(plan.workspace_size, dtype=torch.uint8, device=dev)
     cargs = pa.make_args(q=d["q"], cache_k=d["cache_k"], cache_v=d["cache_v"],
                          k_scale=d["k_scale"], v_scale=d["v_scale"], block_table=d["block_table"],
-                         out=d["out"], lse=d["lse"])
+                         out=d["out"], lse=d["lse"], seq_lens=d["seq_lens"],
+                         seq_lens_kv=d["seq_lens_kv"], cu_seqlens_q=d["cu_seqlens_q"],
+                         attn_mask=d.get("attn_mask"))
     stream = torch.cuda.current_stream(dev)
     pa.pa_plan_upload(plan, ws, stream)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -475,6 +481,8 @@ def main():
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tree-mask", action="store_true",
+                    help="speculative verify with a seeded draft-tree mask (decode-family workloads)")
     ap.add_argument("--op", default="attention", choices=["attention", "cache-append"],
                     help="attention: the path (default); cache-append: the quantise-and-write "
                          "step before it, on the workload's appended tokens")

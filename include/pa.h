@@ -120,6 +120,15 @@ typedef struct pa_args {
   const int32_t* cu_seqlens_q;
   void* out;
   float* lse;
+  /* optional speculative tree mask, uint8 [bsz][M][M] with M = max(seq_lens):
+   * appended token i of sequence b sees appended token j (position
+   * seq_lens_kv[b] + j) only if attn_mask[(b * M + i) * M + j] != 0, in
+   * addition to the causal bound (entries above the diagonal are ignored;
+   * the cached prefix stays visible).  FastDeploy
+   * append_attention_c8_impl.cuh, attn_mask of the speculative-decoding
+   * path.  NULL = plain causal.  Decode family (q_len * G <= 64) with
+   * causal = 1 only; needs cu_seqlens_q. */
+  const uint8_t* attn_mask;
 } pa_args;
 
 typedef struct pa_plan pa_plan_t;

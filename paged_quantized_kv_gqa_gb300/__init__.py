@@ -40,7 +40,7 @@ class PaProblem(ctypes.Structure):
 class PaArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "q", "cache_k", "cache_v", "k_scale", "v_scale", "block_table", "seq_lens",
-        "seq_lens_kv", "cu_seqlens_q", "out", "lse")]
+        "seq_lens_kv", "cu_seqlens_q", "out", "lse", "attn_mask")]
 
 
 class PaPlanDesc(ctypes.Structure):
@@ -195,12 +195,13 @@ def pa_plan(problem: PaProblem, seq_lens, seq_lens_kv, cu_seqlens_q, num_sms: in
 
 
 def make_args(*, q, cache_k, cache_v, k_scale, v_scale, block_table, out, lse=None,
-              seq_lens=None, seq_lens_kv=None, cu_seqlens_q=None) -> PaArgs:
+              seq_lens=None, seq_lens_kv=None, cu_seqlens_q=None, attn_mask=None) -> PaArgs:
     a = PaArgs()
     a.q, a.cache_k, a.cache_v = _ptr(q), _ptr(cache_k), _ptr(cache_v)
     a.k_scale, a.v_scale, a.block_table = _ptr(k_scale), _ptr(v_scale), _ptr(block_table)
     a.seq_lens, a.seq_lens_kv, a.cu_seqlens_q = _ptr(seq_lens), _ptr(seq_lens_kv), _ptr(cu_seqlens_q)
     a.out, a.lse = _ptr(out), _ptr(lse)
+    a.attn_mask = _ptr(attn_mask)
     return a
 
 

@@ -448,6 +448,15 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   p.trace_ctas = fc.trace_ctas;
   p.trace_tiles = fc.trace_tiles;
   p.sm_scale_log2 = pr.sm_scale * 1.4426950408889634f;
+  p.cu_seqlens_q = args->cu_seqlens_q;
+  p.attn_mask = args->attn_mask;
+  p.mask_dim = plan->max_q;
+  if (args->attn_mask) {
+    if (plan->family != PA_FAMILY_DECODE)
+      return fail(PA_ERR_UNSUPPORTED, "a tree mask is supported for the decode family only");
+    if (!pr.causal) return fail(PA_ERR_INVALID_ARG, "a tree mask needs causal = 1");
+    if (!args->cu_seqlens_q) return fail(PA_ERR_INVALID_ARG, "a tree mask needs cu_seqlens_q");
+  }
 
   cudaError_t e;
   if (plan->family == PA_FAMILY_DECODE) {
@@ -554,6 +563,8 @@ pa_status pa_cache_append(const pa_plan_t* plan, const pa_args* args, const void
     return fail(PA_ERR_INVALID_ARG, "kv_stride smaller than one token's K / V row");
   if (reinterpret_cast<uintptr_t>(k_new) % 2 || reinterpret_cast<uintptr_t>(v_new) % 2)
     return fail(PA_ERR_INVALID_ARG, "new K / V rows must be 2-byte aligned (bf16)");
+  if (reinterpret_cast<uintptr_t>(args->cache_k) % 16 || reinterpret_cast<uintptr_t>(args->cache_v) % 16)
+    return fail(PA_ERR_INVALID_ARG, "caches must be 16-byte aligned");
   cudaError_t e = launch_cache_append(*plan, *args, k_new, v_new, kv_stride,
                                       static_cast<int32_t*>(workspace),
                                       static_cast<cudaStream_t>(stream));

@@ -11,8 +11,9 @@
 // round-to-nearest-even saturated to +-448.
 //
 // One CTA per (sequence, page of the appended range, kv head), thread = head
-// dim: reads of the new rows and writes of K rows are coalesced; each thread
-// writes its own V^T row segment.
+// dim: reads of the new rows and writes of K rows are coalesced, each thread
+// writes its own V^T row segment (16 bytes at a time), and the loads of 16
+// positions are issued before their stores.
 #include "pa_common.cuh"
 
 namespace pa {
@@ -76,13 +77,31 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
   }
   const int t0 = p.cu_seqlens_q[b] + (p0 - start);
   if (p.mla) {
-    // whole latent rows: row pos -> cache[page][pos % 64][0 .. 576)
+    // whole latent rows: row pos -> cache[page][pos % 64][0 .. 576); eight
+    // positions' loads are in flight before any store
     const float s = reinterpret_cast<const float*>(p.k_scale)[0];
-    for (int pos = p0; pos < p1; ++pos) {
-      const __nv_bfloat16* src = p.k_new + (int64_t)(t0 + pos - p0) * p.kv_stride;
-      uint8_t* dst = p.cache_k + ((int64_t)page * kPage + (pos % kPage)) * p.head_dim;
-      for (int d = threadIdx.x; d < p.head_dim; d += kThreads)
-        dst[d] = quantize<FP8>(__bfloat162float(src[d]), s);
+    for (int base = p0; base < p1; base += 8) {
+      const int n = min(8, p1 - base);
+      float x[8][5];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const __nv_bfloat16* src = p.k_new + (int64_t)(t0 + base - p0 + j) * p.kv_stride;
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+          const int d = threadIdx.x + c * kThreads;
+          x[j][c] = (j < n && d < p.head_dim) ? __bfloat162float(src[d]) : 0.0f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= n) break;
+        uint8_t* dst = p.cache_k + ((int64_t)page * kPage + ((base + j) % kPage)) * p.head_dim;
+#pragma unroll
+        for (int c = 0; c < 5; ++c) {
+          const int d = threadIdx.x + c * kThreads;
+          if (d < p.head_dim) dst[d] = quantize<FP8>(x[j][c], s);
+        }
+      }
     }
     return;
   }
@@ -94,12 +113,36 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
   const int64_t slab = (int64_t)page * p.kv_heads + kvh;
   uint8_t* krow = p.cache_k + slab * kPage * 128;
   uint8_t* vrow = p.cache_v + (slab * 128 + d) * kPage;
-  for (int pos = p0; pos < p1; ++pos) {
-    const int64_t t = (int64_t)(t0 + pos - p0);
-    const float xk = __bfloat162float(p.k_new[t * p.kv_stride + (int64_t)kvh * 128 + d]);
-    const float xv = __bfloat162float(p.v_new[t * p.kv_stride + (int64_t)kvh * 128 + d]);
-    krow[(pos % kPage) * 128 + d] = quantize<FP8>(xk, sk);
-    vrow[pos % kPage] = quantize<FP8>(xv, sv);
+  const __nv_bfloat16* kin = p.k_new + (int64_t)kvh * 128 + d;
+  const __nv_bfloat16* vin = p.v_new + (int64_t)kvh * 128 + d;
+  // 16-position chunks aligned to the page's 16-position boundaries: all 32
+  // loads in flight before the stores; a full chunk's 16 V bytes go out as one
+  // 16-byte store into the thread's V^T row
+  for (int base = p0; base < p1;) {
+    const int next = min(p1, (base / 16 + 1) * 16);
+    const int n = next - base;
+    float xk[16], xv[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int64_t t = (int64_t)(t0 + base - p0 + j) * p.kv_stride;
+      xk[j] = j < n ? __bfloat162float(kin[t]) : 0.0f;
+      xv[j] = j < n ? __bfloat162float(vin[t]) : 0.0f;
+    }
+    uint32_t vw[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      if (j < n) {
+        const int off = (base + j) % kPage;
+        krow[off * 128 + d] = quantize<FP8>(xk[j], sk);
+        vw[j >> 2] |= (uint32_t)quantize<FP8>(xv[j], sv) << (8 * (j & 3));
+      }
+    }
+    if (n == 16) {
+      *reinterpret_cast<uint4*>(vrow + base % kPage) = make_uint4(vw[0], vw[1], vw[2], vw[3]);
+    } else {
+      for (int j = 0; j < n; ++j) vrow[(base + j) % kPage] = (uint8_t)(vw[j >> 2] >> (8 * (j & 3)));
+    }
+    base = next;
   }
 }
 

@@ -112,7 +112,7 @@ struct TileCursor {
 
 }  // namespace
 
-template <int NR, int FP8>
+template <int NR, int FP8, bool TREE>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                   const AttnParams p) {
@@ -378,6 +378,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float c_log2 = p.sm_scale_log2 *
           (p.scale_kind == PA_SCALE_PER_CHANNEL ? 1.0f : load_scale(p.k_scale, p.scale_kind, cur.kvh));
       const uint32_t o_col = TM::O0 + (li & 1) * NR + r_lo;
+      // speculative tree mask: the item's first token within its sequence and
+      // the sequence's cached prefix length (appended positions start there)
+      int tok0_local = 0, pre_len = 0;
+      const uint8_t* tmask = nullptr;
+      if constexpr (TREE) {
+        tok0_local = cur.tok0 - p.cu_seqlens_q[cur.b];
+        pre_len = cur.cbase - tok0_local;
+        tmask = p.attn_mask + (int64_t)cur.b * p.mask_dim * p.mask_dim;
+      }
 #pragma unroll
       for (int j = 0; j < NH; ++j) l[j] = 0.0f;
       for (int i = 0; i < cur.ntiles; ++i, ++g) {
@@ -405,12 +414,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---- x = s * c (log2 units), -inf where masked
         const int tpos0 = cur.kv0 + i * kTileTok;
         const int jpos = tpos0 + pos_in_tile;
-        const bool need_mask = (tpos0 + kTileTok > cur.kv1) || (tpos0 + kTileTok - 1 > cur.cbase);
+        const bool need_mask = (tpos0 + kTileTok > cur.kv1) || (tpos0 + kTileTok - 1 > cur.cbase) ||
+                               (TREE && tpos0 + kTileTok > pre_len);
         if (need_mask) {
           const int lim_tok = jpos - cur.cbase;   // visible for rows of token >= lim_tok
+          const bool tree = TREE && jpos >= pre_len && jpos < cur.kv1;
 #pragma unroll
           for (int j = 0; j < NH; ++j) {
-            const bool vis = (jpos < cur.kv1) && (r_lo + j >= lim_tok * G);
+            bool vis = (jpos < cur.kv1) && (r_lo + j >= lim_tok * G);
+            if (tree && vis && r_lo + j < n_rows) {
+              // draft token (row's token) sees appended token jpos - pre_len?
+              const int tl = tok0_local + (r_lo + j) / G;
+              vis = tmask[tl * p.mask_dim + (jpos - pre_len)] != 0;
+            }
             s[j] = vis ? s[j] * c_log2 : -INFINITY;
           }
         } else {
@@ -695,7 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int NR, int FP8>
 static cudaError_t launch_t(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
                             const CUtensorMap& tm_v, cudaStream_t stream) {
-  auto kern = decode_kernel<NR, FP8>;
+  // the tree-mask variant is a separate instantiation so that the plain
+  // causal path carries none of its registers
+  auto kern = p.attn_mask != nullptr ? decode_kernel<NR, FP8, true> : decode_kernel<NR, FP8, false>;
   const int smem = Smem<NR>::kTotal;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;

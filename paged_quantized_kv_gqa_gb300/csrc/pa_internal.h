@@ -94,6 +94,9 @@ struct AttnParams {
   int32_t skip_first_load;
   int32_t q_box_tokens;  // query tokens per TMA box of the item's Q rows (append)
   float sm_scale_log2;   // sm_scale * log2(e)
+  const int32_t* cu_seqlens_q;   // device, needed with a tree mask
+  const uint8_t* attn_mask;      // [bsz][mask_dim][mask_dim] or null
+  int32_t mask_dim;
   uint64_t* trace;       // [trace_ctas][trace_tiles][16] %globaltimer stamps, or null
   int32_t trace_ctas;
   int32_t trace_tiles;

@@ -71,4 +71,6 @@ def to_device(case, device="cuda", generate_on_device=True) -> dict:
     d["cu_seqlens_q"] = torch.from_numpy(case.cu_seqlens_q).to(dev)
     d["out"] = torch.zeros((T, case.q_heads, case.head_dim_v), dtype=torch.bfloat16, device=dev)
     d["lse"] = torch.zeros((T, case.q_heads), dtype=torch.float32, device=dev)
+    if getattr(case, "attn_mask", None) is not None:
+        d["attn_mask"] = torch.from_numpy(np.ascontiguousarray(case.attn_mask, np.uint8)).to(dev)
     return d

@@ -29,7 +29,8 @@ def run_case(case, d=None, sms=None, check=True):
     args = pa.make_args(q=d["q"], cache_k=d["cache_k"], cache_v=d["cache_v"],
                         k_scale=d["k_scale"], v_scale=d["v_scale"], block_table=d["block_table"],
                         out=d["out"], lse=d["lse"], seq_lens=d["seq_lens"],
-                        seq_lens_kv=d["seq_lens_kv"], cu_seqlens_q=d["cu_seqlens_q"])
+                        seq_lens_kv=d["seq_lens_kv"], cu_seqlens_q=d["cu_seqlens_q"],
+                        attn_mask=d.get("attn_mask"))
     pa.pa_plan_upload(plan, ws)
     pa.pa_run(plan, args, ws)
     pa.pa_merge(plan, args, ws)
