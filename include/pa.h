@@ -129,6 +129,22 @@ typedef struct pa_args {
    * path.  NULL = plain causal.  Decode family (q_len * G <= 64) with
    * causal = 1 only; needs cu_seqlens_q. */
   const uint8_t* attn_mask;
+  /* optional output epilogue (FastDeploy append_attention_c8_impl.cuh:
+   * shift_bias / smooth_weight and the int8 output with in_scale and the
+   * quant bounds), applied where a row's final output is written (the
+   * attention kernel for one-chunk rows, pa_merge for split rows):
+   *   v' = (v + shift_bias[h * Dv + d]) * smooth_weight[h * Dv + d]
+   *   out_int8 == 0: out is bf16 [T][Hq][Dv], bf16(v')
+   *   out_int8 == 1: out is int8 [T][Hq][Dv],
+   *       clamp(rint(v' * quant_max_bound * in_scale), quant_min_bound, quant_max_bound)
+   * shift_bias / smooth_weight: bf16 [Hq * Dv] or NULL (no shift / no
+   * smoothing).  All zero / NULL = plain bf16 output.  lse is unaffected. */
+  const void* shift_bias;
+  const void* smooth_weight;
+  int32_t out_int8;
+  float in_scale;
+  float quant_max_bound;
+  float quant_min_bound;
 } pa_args;
 
 typedef struct pa_plan pa_plan_t;

@@ -40,7 +40,10 @@ class PaProblem(ctypes.Structure):
 class PaArgs(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in (
         "q", "cache_k", "cache_v", "k_scale", "v_scale", "block_table", "seq_lens",
-        "seq_lens_kv", "cu_seqlens_q", "out", "lse", "attn_mask")]
+        "seq_lens_kv", "cu_seqlens_q", "out", "lse", "attn_mask", "shift_bias",
+        "smooth_weight")] + [("out_int8", ctypes.c_int32), ("in_scale", ctypes.c_float),
+                             ("quant_max_bound", ctypes.c_float),
+                             ("quant_min_bound", ctypes.c_float)]
 
 
 class PaPlanDesc(ctypes.Structure):
@@ -195,13 +198,18 @@ def pa_plan(problem: PaProblem, seq_lens, seq_lens_kv, cu_seqlens_q, num_sms: in
 
 
 def make_args(*, q, cache_k, cache_v, k_scale, v_scale, block_table, out, lse=None,
-              seq_lens=None, seq_lens_kv=None, cu_seqlens_q=None, attn_mask=None) -> PaArgs:
+              seq_lens=None, seq_lens_kv=None, cu_seqlens_q=None, attn_mask=None,
+              shift_bias=None, smooth_weight=None, out_int8=False, in_scale=1.0,
+              quant_max_bound=127.0, quant_min_bound=-127.0) -> PaArgs:
     a = PaArgs()
     a.q, a.cache_k, a.cache_v = _ptr(q), _ptr(cache_k), _ptr(cache_v)
     a.k_scale, a.v_scale, a.block_table = _ptr(k_scale), _ptr(v_scale), _ptr(block_table)
     a.seq_lens, a.seq_lens_kv, a.cu_seqlens_q = _ptr(seq_lens), _ptr(seq_lens_kv), _ptr(cu_seqlens_q)
     a.out, a.lse = _ptr(out), _ptr(lse)
     a.attn_mask = _ptr(attn_mask)
+    a.shift_bias, a.smooth_weight = _ptr(shift_bias), _ptr(smooth_weight)
+    a.out_int8 = 1 if out_int8 else 0
+    a.in_scale, a.quant_max_bound, a.quant_min_bound = in_scale, quant_max_bound, quant_min_bound
     return a
 
 

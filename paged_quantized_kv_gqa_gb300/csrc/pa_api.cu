@@ -324,9 +324,29 @@ static pa_status make_map_q(CUtensorMap* m, const void* q, uint64_t tokens, uint
   return PA_OK;
 }
 
+static OutEpilogue epilogue_of(const pa_args& a) {
+  OutEpilogue e;
+  e.shift = static_cast<const __nv_bfloat16*>(a.shift_bias);
+  e.smooth = static_cast<const __nv_bfloat16*>(a.smooth_weight);
+  e.int8_out = a.out_int8 ? 1 : 0;
+  e.q_scale = a.quant_max_bound * a.in_scale;
+  e.q_min = a.quant_min_bound;
+  e.q_max = a.quant_max_bound;
+  return e;
+}
+
 static pa_status check_args(const Plan& P, const pa_args* a, bool need_cache) {
   if (!a) return fail(PA_ERR_INVALID_ARG, "null pa_args");
   if (!a->out) return fail(PA_ERR_INVALID_ARG, "null out");
+  if (a->out_int8) {
+    if (!(a->quant_max_bound >= a->quant_min_bound) || a->quant_max_bound > 127.0f ||
+        a->quant_min_bound < -128.0f || !std::isfinite(a->in_scale))
+      return fail(PA_ERR_INVALID_ARG, "int8 output needs -128 <= min_bound <= max_bound <= 127 "
+                                      "and a finite in_scale");
+  }
+  if ((a->shift_bias && reinterpret_cast<uintptr_t>(a->shift_bias) % 2) ||
+      (a->smooth_weight && reinterpret_cast<uintptr_t>(a->smooth_weight) % 2))
+    return fail(PA_ERR_INVALID_ARG, "shift_bias / smooth_weight must be 2-byte aligned (bf16)");
   if (need_cache) {
     if (!a->q || !a->cache_k || !a->cache_v || !a->k_scale || !a->v_scale || !a->block_table)
       return fail(PA_ERR_INVALID_ARG, "null device pointer in pa_args");
@@ -448,6 +468,7 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   p.trace_ctas = fc.trace_ctas;
   p.trace_tiles = fc.trace_tiles;
   p.sm_scale_log2 = pr.sm_scale * 1.4426950408889634f;
+  p.ep = epilogue_of(*args);
   p.cu_seqlens_q = args->cu_seqlens_q;
   p.attn_mask = args->attn_mask;
   p.mask_dim = plan->max_q;
@@ -502,7 +523,7 @@ pa_status pa_merge(const pa_plan_t* plan, const pa_args* args, void* workspace, 
   pa_status s = check_args(*plan, args, false);
   if (s != PA_OK) return s;
   const WsView ws = ws_view(*plan, workspace);
-  cudaError_t e = launch_merge(*plan, ws, static_cast<__nv_bfloat16*>(args->out), args->lse,
+  cudaError_t e = launch_merge(*plan, ws, args->out, args->lse, epilogue_of(*args),
                                static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(PA_ERR_CUDA, std::string("merge: ") + cudaGetErrorString(e));
   return PA_OK;

@@ -443,13 +443,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float vs = pc ? 1.0f : load_scale(p.v_scale, p.scale_kind, m.kvh);
       const int token = m.tok0 + tok;
       const int head = m.kvh * G + (r - tok * G);
-      __nv_bfloat16* dst;
-      if (m.nch == 1) {
-        dst = p.out + ((int64_t)token * p.q_heads + head) * kHeadDim;
-      } else {
-        const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
-        dst = p.part_o + sp * kHeadDim;
-      }
+      // one chunk: the final row (output epilogue applied); several: the
+      // normalised partial row for the merge
+      const bool final_row = m.nch == 1;
+      const int64_t obase = final_row
+          ? ((int64_t)token * p.q_heads + head) * kHeadDim
+          : (((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head) * kHeadDim;
+      const OutEpilogue ep_none{nullptr, nullptr, 0, 1.0f, 0.0f, 0.0f};
       const __nv_bfloat16* vsc =
           reinterpret_cast<const __nv_bfloat16*>(p.v_scale) + m.kvh * kHeadDim;
 #pragma unroll
@@ -458,24 +458,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(o_tm + 16 * c, o);
         tmem_wait_ld();
         if (row_ok) {
-          uint32_t w[8];
+          float a[16];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float a0 = __uint_as_float(o[2 * e]) * inv_l;
-            float a1 = __uint_as_float(o[2 * e + 1]) * inv_l;
-            if (pc) {
-              a0 *= __bfloat162float(vsc[16 * c + 2 * e]);
-              a1 *= __bfloat162float(vsc[16 * c + 2 * e + 1]);
-            } else {
-              a0 *= vs;
-              a1 *= vs;
-            }
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(a0, a1);
-            w[e] = *reinterpret_cast<uint32_t*>(&b2);
-          }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
-          d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          for (int e = 0; e < 16; ++e)
+            a[e] = __uint_as_float(o[e]) * inv_l *
+                   (pc ? __bfloat162float(vsc[16 * c + e]) : vs);
+          if (final_row)
+            ep_store16(p.ep, p.out, obase + 16 * c, head * kHeadDim + 16 * c, a);
+          else
+            ep_store16(ep_none, p.part_o, obase + 16 * c, 0, a);
         }
       }
       if (rr == 0) trace_ev(p, gg - 1, X ? 15 : 14);

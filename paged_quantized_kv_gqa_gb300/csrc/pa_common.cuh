@@ -60,6 +60,41 @@ __device__ __forceinline__ Item load_item(const int32_t* items, int it) {
   return m;
 }
 
+// Output epilogue of one element (index = q_head * Dv + dim into shift / smooth).
+__device__ __forceinline__ float ep_value(const OutEpilogue& e, float v, int idx) {
+  if (e.shift != nullptr) v += __bfloat162float(e.shift[idx]);
+  if (e.smooth != nullptr) v *= __bfloat162float(e.smooth[idx]);
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ep_int8(const OutEpilogue& e, float v) {
+  const float q = fminf(fmaxf(rintf(v * e.q_scale), e.q_min), e.q_max);
+  return (uint32_t)(int32_t)q & 0xFFu;
+}
+
+// Final output of 16 consecutive dims (idx0 = q_head * Dv + first dim) to out
+// element offset o: bf16 (two 16-byte stores) or int8 (one 16-byte store).
+__device__ __forceinline__ void ep_store16(const OutEpilogue& e, void* out, int64_t o, int idx0,
+                                           const float (&v)[16]) {
+  if (e.int8_out) {
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int k = 0; k < 16; ++k) w[k >> 2] |= ep_int8(e, ep_value(e, v[k], idx0 + k)) << (8 * (k & 3));
+    *reinterpret_cast<uint4*>(reinterpret_cast<int8_t*>(out) + o) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(ep_value(e, v[2 * k], idx0 + 2 * k),
+                                                ep_value(e, v[2 * k + 1], idx0 + 2 * k + 1));
+      w[k] = *reinterpret_cast<uint32_t*>(&b2);
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(out) + o);
+    d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+}
+
 // lane-0 arrive after the whole warp finished its part
 __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
   __syncwarp();

@@ -350,13 +350,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < NH; ++j) {
         if (r_lo + j < n_rows) {
           const int head = m.kvh * G + gq;
-          const __nv_bfloat16 val =
-              __float2bfloat16_rn(__uint_as_float(v[j]) * inv[r_lo + j] * vs);
+          const float f = __uint_as_float(v[j]) * inv[r_lo + j] * vs;
           if (m.nch == 1) {
-            p.out[((int64_t)token * p.q_heads + head) * kHeadDim + d] = val;
+            const int64_t o = ((int64_t)token * p.q_heads + head) * kHeadDim + d;
+            const float fe = ep_value(p.ep, f, head * kHeadDim + d);
+            if (p.ep.int8_out)
+              reinterpret_cast<int8_t*>(p.out)[o] = (int8_t)ep_int8(p.ep, fe);
+            else
+              p.out[o] = __float2bfloat16_rn(fe);
           } else {
             const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
-            p.part_o[sp * kHeadDim + d] = val;
+            p.part_o[sp * kHeadDim + d] = __float2bfloat16_rn(f);
           }
         }
         if (++gq == G) {

@@ -68,6 +68,18 @@ struct FaultCfg {
   int32_t trace_tiles;
 };
 
+// Output epilogue applied where a query row's final output is written
+// (FastDeploy append_attention_c8_impl.cuh: shift_bias / smooth_weight
+// [q_heads * Dv] and the int8 output with in_scale and the quant bounds):
+//   v' = (v + shift) * smooth;  bf16(v') or int8 clamp(rint(v' * q_scale), q_min, q_max)
+// with q_scale = quant_max_bound * in_scale.  Split rows apply it in the merge.
+struct OutEpilogue {
+  const __nv_bfloat16* shift;    // or null
+  const __nv_bfloat16* smooth;   // or null
+  int32_t int8_out;
+  float q_scale, q_min, q_max;
+};
+
 // Kernel parameter block for the attention kernels (passed by value).
 struct AttnParams {
   const int32_t* items;
@@ -94,6 +106,7 @@ struct AttnParams {
   int32_t skip_first_load;
   int32_t q_box_tokens;  // query tokens per TMA box of the item's Q rows (append)
   float sm_scale_log2;   // sm_scale * log2(e)
+  OutEpilogue ep;
   const int32_t* cu_seqlens_q;   // device, needed with a tree mask
   const uint8_t* attn_mask;      // [bsz][mask_dim][mask_dim] or null
   int32_t mask_dim;
@@ -114,8 +127,8 @@ cudaError_t launch_mla(const Plan& plan, const AttnParams& p, const CUtensorMap&
 cudaError_t launch_cache_append(const Plan& plan, const pa_args& a, const void* k_new,
                                 const void* v_new, int64_t kv_stride, int32_t* status,
                                 cudaStream_t stream);
-cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
-                         cudaStream_t stream);
+cudaError_t launch_merge(const Plan& plan, const WsView& ws, void* out, float* lse,
+                         const OutEpilogue& ep, cudaStream_t stream);
 cudaError_t launch_gather(const pa_problem& prob, const pa_args& a, int32_t b, int32_t kvh,
                           int32_t pos0, int32_t n, void* dk, void* dv, cudaStream_t stream);
 

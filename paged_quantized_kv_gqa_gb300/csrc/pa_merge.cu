@@ -10,9 +10,8 @@
 // slot (token * max_chunks + c) * q_heads + head.  HBM-bound, CUDA cores.
 #include <cfloat>
 
-#include "pa_internal.h"
+#include "pa_common.cuh"
 #include "pa_index.cuh"
-#include "pa_ptx.cuh"
 
 namespace pa {
 
@@ -23,8 +22,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const int32_t* __restrict__ 
                                                     const __nv_bfloat16* __restrict__ part_o,
                                                     const float* __restrict__ part_m,
                                                     const float* __restrict__ part_d,
-                                                    __nv_bfloat16* __restrict__ out,
-                                                    float* __restrict__ lse) {
+                                                    void* __restrict__ out,
+                                                    float* __restrict__ lse,
+                                                    const OutEpilogue ep) {
   constexpr int kPer = DV / 32;  // elements per lane
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -64,22 +64,33 @@ __global__ void __launch_bounds__(256) merge_kernel(const int32_t* __restrict__ 
     }
   }
   const float inv = W > 0.f ? 1.0f / W : 0.f;
-  __nv_bfloat16* dst = out + ((int64_t)token * q_heads + head) * DV + lane * kPer;
+  // final rows: the output epilogue (shift, smooth, bf16 or int8)
+  const int64_t o = ((int64_t)token * q_heads + head) * DV + lane * kPer;
+  const int e0 = head * DV + lane * kPer;
 #pragma unroll
   for (int k = 0; k < kPer; k += 4) {
-    __nv_bfloat162 a = __floats2bfloat162_rn(acc[k] * inv, acc[k + 1] * inv);
-    __nv_bfloat162 b = __floats2bfloat162_rn(acc[k + 2] * inv, acc[k + 3] * inv);
-    uint2 raw;
-    raw.x = *reinterpret_cast<uint32_t*>(&a);
-    raw.y = *reinterpret_cast<uint32_t*>(&b);
-    *reinterpret_cast<uint2*>(dst + k) = raw;
+    float f[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) f[u] = ep_value(ep, acc[k + u] * inv, e0 + k + u);
+    if (ep.int8_out) {
+      const uint32_t w = ep_int8(ep, f[0]) | (ep_int8(ep, f[1]) << 8) | (ep_int8(ep, f[2]) << 16) |
+                         (ep_int8(ep, f[3]) << 24);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<int8_t*>(out) + o + k) = w;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+      uint2 raw;
+      raw.x = *reinterpret_cast<uint32_t*>(&a);
+      raw.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o + k) = raw;
+    }
   }
   if (lse != nullptr && lane == 0)
     lse[(int64_t)token * q_heads + head] = W > 0.f ? M + __logf(W) : -INFINITY;
 }
 
-cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out, float* lse,
-                         cudaStream_t stream) {
+cudaError_t launch_merge(const Plan& plan, const WsView& ws, void* out, float* lse,
+                         const OutEpilogue& ep, cudaStream_t stream) {
   const int n_merge = (int)plan.merge_tokens.size();
   if (n_merge == 0) return cudaSuccess;
   const int warps = n_merge * plan.prob.q_heads;
@@ -87,11 +98,11 @@ cudaError_t launch_merge(const Plan& plan, const WsView& ws, __nv_bfloat16* out,
   if (plan.prob.head_dim_v == 128) {
     merge_kernel<128><<<blocks, 256, 0, stream>>>(ws.merge_tokens, ws.nch_token, n_merge,
                                                  plan.prob.q_heads, plan.max_chunks, ws.part_o,
-                                                 ws.part_m, ws.part_d, out, lse);
+                                                 ws.part_m, ws.part_d, out, lse, ep);
   } else if (plan.prob.head_dim_v == 512) {
     merge_kernel<512><<<blocks, 256, 0, stream>>>(ws.merge_tokens, ws.nch_token, n_merge,
                                                  plan.prob.q_heads, plan.max_chunks, ws.part_o,
-                                                 ws.part_m, ws.part_d, out, lse);
+                                                 ws.part_m, ws.part_d, out, lse, ep);
   } else {
     return cudaErrorInvalidValue;
   }

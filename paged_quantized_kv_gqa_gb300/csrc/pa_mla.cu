@@ -561,29 +561,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (last) {
           if (!wait_or_abort(&pvdone[g & 1], (g >> 1) & 1, limit, abort_any)) { fail = true; break; }
           tc_fence_after();
-          __nv_bfloat16* dst;
-          if (m.nch == 1) {
-            dst = p.out + ((int64_t)m.tok0 * kRows + h) * kDv;
-          } else {
-            const int64_t sp = ((int64_t)m.tok0 * p.max_chunks + m.chunk) * kRows + h;
-            dst = p.part_o + sp * kDv;
-          }
+          // one chunk: the final row (output epilogue applied); several: the
+          // normalised partial row for the merge
+          const bool final_row = m.nch == 1;
+          const int64_t obase = final_row
+              ? ((int64_t)m.tok0 * kRows + h) * kDv
+              : (((int64_t)m.tok0 * p.max_chunks + m.chunk) * kRows + h) * kDv;
+          const OutEpilogue ep_none{nullptr, nullptr, 0, 1.0f, 0.0f, 0.0f};
           const float f = inv_l * vs;
 #pragma unroll 4
           for (int c = 0; c < kDv / 16; ++c) {
             uint32_t v[16];
             tmem_ld16(t_lane + 16 * c, v);
             tmem_wait_ld();
-            uint32_t w[8];
+            float a[16];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]) * f,
-                                                        __uint_as_float(v[2 * e + 1]) * f);
-              w[e] = *reinterpret_cast<uint32_t*>(&b2);
-            }
-            uint4* d4 = reinterpret_cast<uint4*>(dst + 16 * c);
-            d4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            d4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            for (int e = 0; e < 16; ++e) a[e] = __uint_as_float(v[e]) * f;
+            if (final_row)
+              ep_store16(p.ep, p.out, obase + 16 * c, h * kDv + 16 * c, a);
+            else
+              ep_store16(ep_none, p.part_o, obase + 16 * c, 0, a);
           }
           tc_fence_before();
           if (h == 0) trace_ev(p, g, 12);
