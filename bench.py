@@ -188,7 +188,11 @@ def run_cuda(args) -> dict:
         case.name += " tree-mask"
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     d = to_device(case, dev)
+    if args.fused_merge:
+        pa.pa_set_fused_merge(True)
+        case.name += " fused-merge"
     plan = pa.pa_plan(pa.problem_of(case), case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, sms)
+    pa.pa_set_fused_merge(False)
     desc = plan.describe()
     ws = torch.zeros(plan.workspace_size, dtype=torch.uint8, device=dev)
     cargs = pa.make_args(q=d["q"], cache_k=d["cache_k"], cache_v=d["cache_v"],
@@ -483,6 +487,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tree-mask", action="store_true",
                     help="speculative verify with a seeded draft-tree mask (decode-family workloads)")
+    ap.add_argument("--fused-merge", action="store_true",
+                    help="decode-family workloads: merge split rows inside the attention launch "
+                         "(opt-in single-launch mode) instead of the separate merge kernel")
     ap.add_argument("--op", default="attention", choices=["attention", "cache-append"],
                     help="attention: the path (default); cache-append: the quantise-and-write "
                          "step before it, on the workload's appended tokens")

@@ -158,7 +158,7 @@ typedef struct pa_plan_desc {
   int32_t num_ctas;         /* persistent CTAs (MLA: CTA pairs)               */
   int32_t total_q;          /* T                                              */
   int32_t max_chunks;       /* partial slots per token                        */
-  int32_t n_merge;          /* tokens whose rows need pa_merge                */
+  int32_t n_merge;          /* tokens whose rows are split into chunks        */
   const int32_t* items;     /* [num_items][8]: b, kvh, token0, n_tok,
                                causal_base, kv0, kv1, chunk | (n_chunks << 16)
                                in CTA-major order                            */
@@ -168,6 +168,8 @@ typedef struct pa_plan_desc {
   size_t workspace_bytes;
   int64_t kv_bytes;         /* cache bytes read once: visible (page, head) slabs */
   double flops;             /* 2*(Dqk+Dv) per visible (position, query head)  */
+  int32_t fused_merge;      /* 1: pa_run merges the split rows itself (decode
+                               family), pa_merge does nothing               */
 } pa_plan_desc;
 
 /*
@@ -206,13 +208,20 @@ pa_status pa_plan_upload(const pa_plan_t* plan, void* workspace, void* stream);
  * item; MLA: one query token per item on a 2-CTA cluster; append and MLA need
  * out 16-byte aligned).  Items that cover the whole KV range of
  * their rows write out/lse directly; split rows write partial states into the
- * workspace and need pa_merge afterwards.  The workspace must hold this plan
- * (pa_plan_upload).  PA_ERR_UNSUPPORTED for a family whose kernel is not
- * compiled into this build. */
+ * workspace.  Decode-family plans built with pa_set_fused_merge(1)
+ * (pa_plan_desc.fused_merge = 1) also merge them in the same launch: the CTA that writes a row group's last chunk
+ * merges it (FastDeploy append_attention_c8_impl.cuh merge step, FlashInfer
+ * persistent.cuh reduction, XQA mla_sm120.cu "last CTA merges" semaphore)
+ * and resets the group's counter in the workspace, so the uploaded plan
+ * stays valid for the next pa_run; after a failed run (pa_check != PA_OK)
+ * upload the plan again.  Other plans need pa_merge afterwards.  The
+ * workspace must hold this plan (pa_plan_upload).  PA_ERR_UNSUPPORTED for a
+ * family whose kernel is not compiled into this build. */
 pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, void* stream);
 
 /* Enqueues the log-sum-exp merge of the partial states of split rows into
- * out/lse.  A no-op when the plan has no split rows. */
+ * out/lse.  A no-op when the plan has no split rows or merges them inside
+ * pa_run (pa_plan_desc.fused_merge). */
 pa_status pa_merge(const pa_plan_t* plan, const pa_args* args, void* workspace, void* stream);
 
 /* Synchronises the stream, then reads the workspace status word.  Returns
@@ -303,6 +312,17 @@ pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load);
  * Process-wide setting.
  */
 pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta);
+
+/*
+ * Opt-in single-launch path: with on = 1, decode-family plans built
+ * afterwards merge their split rows inside pa_run (two warps of each CTA;
+ * the CTA that writes a row group's last chunk merges it) and pa_merge does
+ * nothing for them.  Default 0: pa_merge's separate kernel is faster on
+ * GB300, because the in-kernel merge's chains of dependent partial-state
+ * loads queue behind the attention kernel's own page stream.  Process-wide
+ * setting, read by pa_plan.
+ */
+pa_status pa_set_fused_merge(int32_t on);
 
 #ifdef __cplusplus
 }

@@ -56,7 +56,8 @@ class PaPlanDesc(ctypes.Structure):
         ("merge_tokens", ctypes.POINTER(ctypes.c_int32)),
         ("workspace_bytes", ctypes.c_size_t),
         ("kv_bytes", ctypes.c_int64),
-        ("flops", ctypes.c_double)]
+        ("flops", ctypes.c_double),
+        ("fused_merge", ctypes.c_int32)]
 
 
 def _load():
@@ -82,6 +83,7 @@ def _load():
         "pa_debug_set_faults": ([i64, i32], i32),
         "pa_run_static": ([vp, ctypes.POINTER(PaArgs), vp, i32], i32),
         "pa_debug_set_trace": ([vp, i32, i32], i32),
+        "pa_set_fused_merge": ([i32], i32),
         "pa_cache_append": ([vp, ctypes.POINTER(PaArgs), vp, vp, i64, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
@@ -179,7 +181,7 @@ class Plan:
                     nch_token=arr(d.nch_token, d.total_q),
                     merge_tokens=arr(d.merge_tokens, d.n_merge),
                     workspace_bytes=int(d.workspace_bytes), kv_bytes=int(d.kv_bytes),
-                    flops=float(d.flops))
+                    flops=float(d.flops), fused_merge=bool(d.fused_merge))
 
     @property
     def workspace_size(self) -> int:
@@ -262,6 +264,12 @@ def pa_debug_set_trace(buf=None, ctas: int = 0, tiles_per_cta: int = 0):
     """Enable (device uint64 buffer of ctas * tiles_per_cta * 16) or disable (None)
     the kernels' %globaltimer pipeline trace."""
     _check(lib.pa_debug_set_trace(_ptr(buf), int(ctas), int(tiles_per_cta)))
+
+
+def pa_set_fused_merge(on: bool):
+    """Decode-family plans built afterwards merge split rows inside pa_run (True)
+    or leave them to pa_merge's separate kernel (False, the default)."""
+    _check(lib.pa_set_fused_merge(1 if on else 0))
 
 
 def pa_last_error() -> str:

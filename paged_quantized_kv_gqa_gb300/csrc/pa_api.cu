@@ -27,7 +27,7 @@
 namespace pa {
 
 static thread_local std::string g_last_error;
-static FaultCfg g_faults{kDefaultWaitNs, 0, nullptr, 0, 0};
+static FaultCfg g_faults{kDefaultWaitNs, 0, nullptr, 0, 0, 0};
 static std::mutex g_fault_mu;
 
 void set_error(const std::string& msg) { g_last_error = msg; }
@@ -217,7 +217,12 @@ static pa_status build_plan(const pa_problem& prob, const int32_t* ql, const int
   P.off_items = align4(P.off_indptr + P.work_indptr.size());
   P.off_nch = align4(P.off_items + P.items.size());
   P.off_merge = align4(P.off_nch + P.nch_token.size());
-  const size_t words = P.off_merge + P.merge_tokens.size();
+  {
+    std::lock_guard<std::mutex> lk(g_fault_mu);
+    P.fused_merge = P.family == PA_FAMILY_DECODE && !P.merge_tokens.empty() && g_faults.fused_merge;
+  }
+  P.off_cnt = align4(P.off_merge + P.merge_tokens.size());
+  const size_t words = P.off_cnt + (P.fused_merge ? (size_t)P.total_q * prob.kv_heads : 0);
   static_assert(kStatusBytes % 16 == 0, "plan blob must start 16-byte aligned");
   P.blob.assign(std::max<size_t>(words, 1), 0);
   std::copy(P.work_indptr.begin(), P.work_indptr.end(), P.blob.begin() + P.off_indptr);
@@ -263,6 +268,8 @@ static WsView ws_view(const Plan& P, void* ws) {
   v.items = blob + P.off_items;
   v.nch_token = blob + P.off_nch;
   v.merge_tokens = blob + P.off_merge;
+  v.merge_cnt = P.fused_merge
+                    ? reinterpret_cast<int32_t*>(base + kStatusBytes) + P.off_cnt : nullptr;
   v.part_o = reinterpret_cast<__nv_bfloat16*>(base + P.part_o_off);
   v.part_m = reinterpret_cast<float*>(base + P.part_m_off);
   v.part_d = reinterpret_cast<float*>(base + P.part_d_off);
@@ -408,6 +415,7 @@ pa_status pa_plan_describe(const pa_plan_t* plan, pa_plan_desc* d) {
   d->workspace_bytes = plan->ws_bytes;
   d->kv_bytes = plan->kv_bytes;
   d->flops = plan->flops;
+  d->fused_merge = plan->fused_merge ? 1 : 0;
   return PA_OK;
 }
 
@@ -464,6 +472,7 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   p.scale_kind = pr.scale_kind;
   p.max_chunks = plan->max_chunks;
   p.skip_first_load = fc.skip_first_load;
+  p.merge_cnt = ws.merge_cnt;
   p.trace = fc.trace;
   p.trace_ctas = fc.trace_ctas;
   p.trace_tiles = fc.trace_tiles;
@@ -522,6 +531,7 @@ pa_status pa_merge(const pa_plan_t* plan, const pa_args* args, void* workspace, 
   if (!plan || !workspace) return fail(PA_ERR_INVALID_ARG, "null plan or workspace");
   pa_status s = check_args(*plan, args, false);
   if (s != PA_OK) return s;
+  if (plan->fused_merge) return PA_OK;   // pa_run merged the split rows
   const WsView ws = ws_view(*plan, workspace);
   cudaError_t e = launch_merge(*plan, ws, args->out, args->lse, epilogue_of(*args),
                                static_cast<cudaStream_t>(stream));
@@ -598,6 +608,12 @@ pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load) {
   std::lock_guard<std::mutex> lk(g_fault_mu);
   g_faults.wait_limit_ns = wait_limit_ns == 0 ? kDefaultWaitNs : wait_limit_ns;
   g_faults.skip_first_load = skip_first_load ? 1 : 0;
+  return PA_OK;
+}
+
+pa_status pa_set_fused_merge(int32_t on) {
+  std::lock_guard<std::mutex> lk(g_fault_mu);
+  g_faults.fused_merge = on ? 1 : 0;
   return PA_OK;
 }
 

@@ -21,9 +21,16 @@
 //       CV        Q' of each item, K rows (lane = position) and V^T rows (lane
 //                 = head dim) dequantised straight into TMEM;
 //       IO        one TMA warp ((page, kv head) K slab [64 x 128] with 128B
-//                 swizzle and V slab [128 x 64] with 64B swizzle per page) and
+//                 swizzle and V slab [128 x 64] with 64B swizzle per page),
 //                 one MMA warp issuing S = K Q'^T and O += V^T P^T, polling
-//                 both queues and issuing whichever is ready.
+//                 both queues and issuing whichever is ready, and two merge
+//                 warps, active only in the opt-in single-launch mode: for
+//                 split rows the CTA that wrote a row group's last chunk
+//                 merges the group's partial states (a per-group counter in
+//                 the workspace, as the pages' "last CTA merges" semaphore).
+//                 Off by default: those merges' dependent loads queue behind
+//                 the kernel's own page stream, and the separate merge kernel
+//                 is faster.
 //     The roles meet only at mbarriers: K, V and S are double-buffered, P^T
 //     four-deep, Q' and O double-buffered per item (the epilogue of an item
 //     runs during the next item), so dequantisation, softmax, tensor-core work
@@ -40,6 +47,7 @@
 
 #include "pa_common.cuh"
 #include "pa_index.cuh"
+#include "pa_merge.cuh"
 
 namespace pa {
 namespace {
@@ -55,6 +63,7 @@ constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBufs = 4;                        // P^T ring depth
+constexpr int kMergeRows = 2;                    // rows a merge warp combines at once
 
 // The decode pipeline is latency-bound: its waits re-probe every 32 ns.
 __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
@@ -85,7 +94,8 @@ struct Smem {
   // full[S], empty[S], kready[2], sfull[2], sfree[2], pready[4], vready[2], pvdone[4]
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + kPBufs + 2 + kPBufs;
   static constexpr int kMisc = kBars + kNumBars * 8;       // tmem addr, abort flags
-  static constexpr int kTotal = kMisc + 32 + 1024;         // + alignment slack
+  static constexpr int kEpDone = kMisc + 32;               // [8] items finished per softmax warp
+  static constexpr int kTotal = kEpDone + 32 + 1024;       // + alignment slack
   static_assert(kTotal <= 232448, "shared memory overflow");
 };
 
@@ -135,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
   volatile int* abort_any = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
   volatile int* abort_grp = reinterpret_cast<volatile int*>(smem + SM::kMisc + 8);  // [2]
+  volatile int* ep_done = reinterpret_cast<volatile int*>(smem + SM::kEpDone);      // [8]
   float* red = reinterpret_cast<float*>(smem + SM::kRed);
   float* red_l = reinterpret_cast<float*>(smem + SM::kRedL);
   float* lsum_s = reinterpret_cast<float*>(smem + SM::kLsum);
@@ -171,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_any = 0;
     abort_grp[0] = 0;
     abort_grp[1] = 0;
+    for (int w = 0; w < 8; ++w) ep_done[w] = 0;
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
@@ -308,7 +320,64 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (pv_commits[j]) mbar_wait(&pvdone[j], (pv_commits[j] - 1) & 1, limit);
     }
   } else if (wg == 3) {
-    // warps 14-15: no role (they complete the fourth warpgroup)
+    // ================================================================ fused merge
+    // warps 14 and 15 take alternate items; once all eight softmax warps have
+    // finished an item's epilogue, its row group's counter is raised and the
+    // CTA that completes the count merges the group and resets the counter
+    if (p.merge_cnt != nullptr) {
+      bool ok = true;
+      for (int it = item_begin + (warp - 14); it < item_end && ok; it += 2) {
+        const int li = it - item_begin;
+        const uint64_t t0 = globaltimer();
+        while (true) {
+          const bool done = lane >= 8 || ep_done[lane] > li;
+          if (__all_sync(0xffffffffu, done)) break;
+          const bool give_up = *abort_any || globaltimer() - t0 > limit;
+          if (__shfl_sync(0xffffffffu, give_up, 0)) { ok = false; break; }
+          __nanosleep(128);
+        }
+        if (!ok) break;
+        __threadfence_block();   // acquire the epilogue's partial-state writes
+        const Item m = load_item<kTileTok>(p.items, it);
+        if (m.nch <= 1) continue;
+        int32_t* cnt = p.merge_cnt + (int64_t)m.tok0 * p.kv_heads + m.kvh;
+        int prev = 0;
+        if (lane == 0) {
+          __threadfence();        // this CTA's partial states before its count
+          prev = atomicAdd(cnt, 1);
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev != m.nch - 1) continue;
+        __threadfence();          // every chunk's partial states after the last count
+        const int rows = m.ntok * G;
+        for (int r0 = 0; r0 < rows; r0 += kMergeRows) {
+          int64_t slot0[kMergeRows];
+          bool valid[kMergeRows];
+          int tok[kMergeRows], head[kMergeRows];
+#pragma unroll
+          for (int r = 0; r < kMergeRows; ++r) {
+            const int rr = min(r0 + r, rows - 1);
+            valid[r] = r0 + r < rows;
+            tok[r] = m.tok0 + rr / G;
+            head[r] = m.kvh * G + rr % G;
+            slot0[r] = (int64_t)tok[r] * p.max_chunks * p.q_heads + head[r];
+          }
+          float acc[kMergeRows][kHeadDim / 32], M[kMergeRows], W[kMergeRows];
+          merge_rows<kHeadDim, kMergeRows>(p.part_o, p.part_m, p.part_d, slot0, valid, p.q_heads, m.nch,
+                                  lane, acc, M, W);
+#pragma unroll
+          for (int r = 0; r < kMergeRows; ++r)
+            if (valid[r])
+              merge_store<kHeadDim>(acc[r], M[r], W[r], p.out, p.lse, p.ep, tok[r], head[r],
+                                    p.q_heads, lane);
+        }
+        if (lane == 0) *cnt = 0;  // the group is done: ready for the next launch
+      }
+      if (!ok && lane == 0) {
+        if (!*abort_any) record_status(p.status, PA_ERR_DEVICE_TIMEOUT, item_begin);
+        *abort_any = 1;
+      }
+    }
   } else if (wg < 2) {
     // ================================================================ softmax
     // warpgroup wg owns packed rows [r_lo, r_lo + NH); lane = position
@@ -366,6 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++gq == G) {
           gq = 0;
           ++token;
+        }
+      }
+      if (p.merge_cnt != nullptr) {
+        // publish: this warp's rows of item li are written (release to the merge warps)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          ep_done[warp] = li + 1;
         }
       }
       if (tid == 0) trace_ev(p, gl, 10);

@@ -37,10 +37,15 @@ struct Plan {
   std::vector<int32_t> work_indptr;  // [num_ctas+1]
   std::vector<int32_t> nch_token;    // [T]
   std::vector<int32_t> merge_tokens; // [n_merge]
-  // device blob = work_indptr | items | nch_token | merge_tokens (int32), at kStatusBytes;
-  // each array starts at a multiple of 4 words (16 bytes)
+  // split rows of a decode-family plan are merged inside the attention kernel
+  // (the CTA that finishes a row group's last chunk merges it); pa_merge is
+  // then a no-op
+  bool fused_merge = false;
+  // device blob = work_indptr | items | nch_token | merge_tokens | merge
+  // counters [total_q][kv_heads] (zeros; fused merge only) (int32), at
+  // kStatusBytes; each array starts at a multiple of 4 words (16 bytes)
   std::vector<int32_t> blob;
-  size_t off_indptr = 0, off_items = 0, off_nch = 0, off_merge = 0;  // int32 offsets in blob
+  size_t off_indptr = 0, off_items = 0, off_nch = 0, off_merge = 0, off_cnt = 0;  // int32 offsets
   size_t plan_bytes = 0;
   size_t part_o_off = 0, part_m_off = 0, part_d_off = 0, ws_bytes = 0;  // byte offsets
   int64_t kv_bytes = 0;
@@ -55,6 +60,7 @@ struct WsView {
   const int32_t* items;
   const int32_t* nch_token;
   const int32_t* merge_tokens;
+  int32_t* merge_cnt;   // fused merge counters or null
   __nv_bfloat16* part_o;
   float* part_m;
   float* part_d;
@@ -66,6 +72,7 @@ struct FaultCfg {
   uint64_t* trace;        // device timeline buffer or null
   int32_t trace_ctas;
   int32_t trace_tiles;
+  int32_t fused_merge;    // plans built while 1 merge decode split rows in-kernel (default 0)
 };
 
 // Output epilogue applied where a query row's final output is written
@@ -110,6 +117,7 @@ struct AttnParams {
   const int32_t* cu_seqlens_q;   // device, needed with a tree mask
   const uint8_t* attn_mask;      // [bsz][mask_dim][mask_dim] or null
   int32_t mask_dim;
+  int32_t* merge_cnt;    // [total_q][kv_heads] fused-merge counters (decode), or null
   uint64_t* trace;       // [trace_ctas][trace_tiles][16] %globaltimer stamps, or null
   int32_t trace_ctas;
   int32_t trace_tiles;

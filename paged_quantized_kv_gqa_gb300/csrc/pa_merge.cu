@@ -1,17 +1,15 @@
 // pa_merge.cu - split-KV partial-state merge and the raw-gather test hook.
 //
 // Merge (FastDeploy append_attention_c8_impl.cuh, merge_multi_chunks_*_kernel
-// launched after the split kernel; FlashInfer persistent.cuh,
-// BlockBatchReductionPersistent; XQA mla_sm120.cu, mergePartialOutputs):
-// for a query row with chunk states (o_c, m_c, d_c), o_c normalised,
-//   M = max_c m_c,  w_c = d_c * exp(m_c - M),
-//   out = sum_c w_c o_c / sum_c w_c,  lse = M + log(sum_c w_c).
+// launched after the split kernel; the arithmetic is in pa_merge.cuh).
 // One warp per (token, query head); the partial states of a token sit at
-// slot (token * max_chunks + c) * q_heads + head.  HBM-bound, CUDA cores.
+// slot (token * max_chunks + c) * q_heads + head.  HBM-bound, CUDA cores:
+// the row reads of all chunks are issued before they are summed.
 #include <cfloat>
 
 #include "pa_common.cuh"
 #include "pa_index.cuh"
+#include "pa_merge.cuh"
 
 namespace pa {
 
@@ -25,68 +23,17 @@ __global__ void __launch_bounds__(256) merge_kernel(const int32_t* __restrict__ 
                                                     void* __restrict__ out,
                                                     float* __restrict__ lse,
                                                     const OutEpilogue ep) {
-  constexpr int kPer = DV / 32;  // elements per lane
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= n_merge * q_heads) return;
   const int token = merge_tokens[wid / q_heads];
   const int head = wid % q_heads;
   const int nch = nch_token[token];
-  const int64_t slot0 = (int64_t)token * max_chunks * q_heads + head;
-
-  float M = -INFINITY;
-  for (int c = lane; c < nch; c += 32) M = fmaxf(M, part_m[slot0 + (int64_t)c * q_heads]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-
-  float acc[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
-  float W = 0.f;
-  if (M != -INFINITY) {
-    for (int c = 0; c < nch; ++c) {
-      const int64_t slot = slot0 + (int64_t)c * q_heads;
-      const float mc = part_m[slot];
-      if (mc == -INFINITY) continue;
-      const float w = part_d[slot] * __expf(mc - M);
-      W += w;
-      const __nv_bfloat16* src = part_o + slot * DV + lane * kPer;
-#pragma unroll
-      for (int k = 0; k < kPer; k += 4) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src + k);
-        const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-        const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-        acc[k + 0] += w * __low2float(a);
-        acc[k + 1] += w * __high2float(a);
-        acc[k + 2] += w * __low2float(b);
-        acc[k + 3] += w * __high2float(b);
-      }
-    }
-  }
-  const float inv = W > 0.f ? 1.0f / W : 0.f;
-  // final rows: the output epilogue (shift, smooth, bf16 or int8)
-  const int64_t o = ((int64_t)token * q_heads + head) * DV + lane * kPer;
-  const int e0 = head * DV + lane * kPer;
-#pragma unroll
-  for (int k = 0; k < kPer; k += 4) {
-    float f[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) f[u] = ep_value(ep, acc[k + u] * inv, e0 + k + u);
-    if (ep.int8_out) {
-      const uint32_t w = ep_int8(ep, f[0]) | (ep_int8(ep, f[1]) << 8) | (ep_int8(ep, f[2]) << 16) |
-                         (ep_int8(ep, f[3]) << 24);
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<int8_t*>(out) + o + k) = w;
-    } else {
-      __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
-      __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
-      uint2 raw;
-      raw.x = *reinterpret_cast<uint32_t*>(&a);
-      raw.y = *reinterpret_cast<uint32_t*>(&b);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o + k) = raw;
-    }
-  }
-  if (lse != nullptr && lane == 0)
-    lse[(int64_t)token * q_heads + head] = W > 0.f ? M + __logf(W) : -INFINITY;
+  const int64_t slot0[1] = {(int64_t)token * max_chunks * q_heads + head};
+  const bool valid[1] = {true};
+  float acc[1][DV / 32], M[1], W[1];
+  merge_rows<DV, 1>(part_o, part_m, part_d, slot0, valid, q_heads, nch, lane, acc, M, W);
+  merge_store<DV>(acc[0], M[0], W[0], out, lse, ep, token, head, q_heads, lane);
 }
 
 cudaError_t launch_merge(const Plan& plan, const WsView& ws, void* out, float* lse,

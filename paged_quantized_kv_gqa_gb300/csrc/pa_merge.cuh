@@ -1,0 +1,145 @@
+// pa_merge.cuh - merge of split-KV partial states (device functions shared by
+// the merge kernel and the decode kernel's fused merge).
+//
+// FastDeploy append_attention_c8_impl.cuh (merge_multi_chunks kernels),
+// FlashInfer persistent.cuh (BlockBatchReductionPersistent), XQA
+// mla_sm120.cu (mergePartialOutputs): for a query row with chunk states
+// (o_c, m_c, d_c), o_c normalised,
+//   M = max_c m_c,  w_c = d_c exp(m_c - M),
+//   out = sum_c w_c o_c / sum_c w_c,  lse = M + log(sum_c w_c).
+// Chunk c of a row sits at slot slot0 + c * cstride of part_m / part_d and at
+// part_o + (slot0 + c * cstride) * DV.
+#pragma once
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+// Merges R rows with one warp (all lanes call it; rows with valid[r] false
+// come out with W = 0).  The partial states are read through L2 only (other
+// CTAs of the same launch may have written them).  Lane l owns output elements [l * DV / 32, + DV / 32);
+// lane c holds the weight of chunk c0 + c, and each row's chunk vectors are
+// read four chunks at a time so that their loads are in flight together.
+template <int DV, int R>
+__device__ __forceinline__ void merge_rows(const __nv_bfloat16* __restrict__ part_o,
+                                           const float* __restrict__ part_m,
+                                           const float* __restrict__ part_d,
+                                           const int64_t (&slot0)[R], const bool (&valid)[R],
+                                           int64_t cstride, int nch, int lane,
+                                           float (&acc)[R][DV / 32], float (&M)[R], float (&W)[R]) {
+  constexpr int kPer = DV / 32;
+  static_assert(kPer % 4 == 0, "lane slice must be a multiple of 4 elements");
+  float m0[R], d0[R];   // chunk `lane` of each row (the first pass of 32)
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    m0[r] = -INFINITY;
+    d0[r] = 0.f;
+    if (valid[r] && lane < nch) {
+      m0[r] = __ldcg(part_m + slot0[r] + lane * cstride);
+      d0[r] = __ldcg(part_d + slot0[r] + lane * cstride);
+    }
+    M[r] = m0[r];
+  }
+  for (int c = lane + 32; c < nch; c += 32) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (valid[r]) M[r] = fmaxf(M[r], __ldcg(part_m + slot0[r] + c * cstride));
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M[r] = fmaxf(M[r], __shfl_xor_sync(0xffffffffu, M[r], o));
+    W[r] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[r][k] = 0.f;
+  }
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    float w[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      float mc = m0[r], dc = d0[r];
+      if (c0 > 0) {
+        mc = -INFINITY;
+        if (valid[r] && c0 + lane < nch) {
+          mc = __ldcg(part_m + slot0[r] + (c0 + lane) * cstride);
+          dc = __ldcg(part_d + slot0[r] + (c0 + lane) * cstride);
+        }
+      }
+      w[r] = (mc != -INFINITY) ? dc * __expf(mc - M[r]) : 0.f;
+      W[r] += w[r];
+    }
+    const int n = min(32, nch - c0);
+    for (int j = 0; j < n; j += 4) {
+      float wj[R][4];
+      uint2 raw[R][4][kPer / 4];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          wj[r][u] = __shfl_sync(0xffffffffu, w[r], (j + u) & 31);
+          const __nv_bfloat16* src =
+              part_o + (slot0[r] + (c0 + j + u) * cstride) * DV + lane * kPer;
+#pragma unroll
+          for (int k = 0; k < kPer / 4; ++k)
+            raw[r][u][k] = (j + u < n && wj[r][u] != 0.f)
+                               ? __ldcg(reinterpret_cast<const uint2*>(src + 4 * k))
+                               : make_uint2(0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+          for (int k = 0; k < kPer / 4; ++k) {
+            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw[r][u][k].x);
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw[r][u][k].y);
+            acc[r][4 * k + 0] += wj[r][u] * __low2float(a);
+            acc[r][4 * k + 1] += wj[r][u] * __high2float(a);
+            acc[r][4 * k + 2] += wj[r][u] * __low2float(b);
+            acc[r][4 * k + 3] += wj[r][u] * __high2float(b);
+          }
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) W[r] += __shfl_xor_sync(0xffffffffu, W[r], o);
+  }
+}
+
+// Final output of a merged row (output epilogue applied) and its lse.
+template <int DV>
+__device__ __forceinline__ void merge_store(const float (&acc)[DV / 32], float M, float W,
+                                            void* __restrict__ out, float* __restrict__ lse,
+                                            const OutEpilogue& ep, int token, int head,
+                                            int q_heads, int lane) {
+  constexpr int kPer = DV / 32;
+  const float inv = W > 0.f ? 1.0f / W : 0.f;
+  const int64_t o = ((int64_t)token * q_heads + head) * DV + lane * kPer;
+  const int e0 = head * DV + lane * kPer;
+#pragma unroll
+  for (int k = 0; k < kPer; k += 4) {
+    float f[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) f[u] = ep_value(ep, acc[k + u] * inv, e0 + k + u);
+    if (ep.int8_out) {
+      const uint32_t w = ep_int8(ep, f[0]) | (ep_int8(ep, f[1]) << 8) | (ep_int8(ep, f[2]) << 16) |
+                         (ep_int8(ep, f[3]) << 24);
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<int8_t*>(out) + o + k) = w;
+    } else {
+      __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+      uint2 raw;
+      raw.x = *reinterpret_cast<uint32_t*>(&a);
+      raw.y = *reinterpret_cast<uint32_t*>(&b);
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + o + k) = raw;
+    }
+  }
+  if (lse != nullptr && lane == 0)
+    lse[(int64_t)token * q_heads + head] = W > 0.f ? M + __logf(W) : -INFINITY;
+}
+
+}  // namespace pa

@@ -97,6 +97,23 @@ def test_workspace_and_work_counts(pa):
     assert d["workspace_bytes"] >= T * d["max_chunks"] * H * (128 * 2 + 8)
 
 
+def test_fused_merge_only_for_split_decode_plans(pa):
+    """With the single-launch option on, decode-family plans with split rows
+    merge inside the attention launch; append / MLA plans and unsplit plans
+    never do, and the option is off by default."""
+    assert not _plan(pa, synth.config(2)).describe()["fused_merge"]     # default off
+    pa.pa_set_fused_merge(True)
+    try:
+        assert _plan(pa, synth.config(2)).describe()["fused_merge"]
+        assert _plan(pa, synth.config(4)).describe()["fused_merge"]
+        assert not _plan(pa, synth.config(1)).describe()["fused_merge"]     # no split
+        assert not _plan(pa, synth.config(3)).describe()["fused_merge"]     # append
+        assert not _plan(pa, synth.config(5)).describe()["fused_merge"]     # MLA
+    finally:
+        pa.pa_set_fused_merge(False)
+    assert not _plan(pa, synth.config(2)).describe()["fused_merge"]
+
+
 @pytest.mark.parametrize("field,value,status", [
     ("chunk_size", 100, 1),        # not a multiple of the page size
     ("q_heads", 30, 1),            # not a multiple of kv_heads
