@@ -469,6 +469,9 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   p.q_heads = pr.q_heads;
   p.kv_heads = pr.kv_heads;
   p.group = pr.q_heads / pr.kv_heads;
+  // decode: when every item's packed rows fit in the first half of the tile,
+  // the second softmax warpgroup would only process padding rows
+  p.softmax_wgs = (plan->max_q * p.group <= plan->decode_rows / 2) ? 1 : 2;
   p.scale_kind = pr.scale_kind;
   p.max_chunks = plan->max_chunks;
   p.skip_first_load = fc.skip_first_load;

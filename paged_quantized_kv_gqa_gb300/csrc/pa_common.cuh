@@ -5,12 +5,6 @@
 #include <cstdint>
 
 #include "pa_internal.h"
-
-#ifdef PA_INLINE_COLD
-#define PA_COLD __forceinline__
-#else
-#define PA_COLD __noinline__
-#endif
 #include "pa_ptx.cuh"
 
 namespace pa {
@@ -39,24 +33,6 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
     if (*abort_any) return false;
     if (globaltimer() - t0 > limit_ns) return false;
   }
-}
-
-// The same wait with its polling loop out of line: a call site costs one
-// probe and a branch, which keeps latency-bound kernels' hot loops short.
-static __device__ PA_COLD bool wait_slow(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                              volatile int* abort_any, uint32_t hint_ns) {
-  const uint64_t t0 = globaltimer();
-  while (true) {
-    if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
-    if (*abort_any) return false;
-    if (globaltimer() - t0 > limit_ns) return false;
-  }
-}
-
-__device__ __forceinline__ bool wait_or_abort_ool(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
-                                                  volatile int* abort_any, uint32_t hint_ns) {
-  if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
-  return wait_slow(bar, parity, limit_ns, abort_any, hint_ns);
 }
 
 // Scale value `idx` (kv head or kv_head * D + channel) of a bf16 scale array,
@@ -88,29 +64,6 @@ __device__ __forceinline__ Item load_item(const int32_t* items, int it) {
   return item_from<TILE>(r[0], r[1]);
 }
 
-// A CTA's work items, the first `cap` of them staged in shared memory at
-// kernel start so that no role waits on a global load at an item boundary.
-struct ItemTable {
-  const int4* s;          // shared copy: two int4 per item
-  const int32_t* g;       // global list
-  int begin, cap;
-  template <int TILE>
-  __device__ __forceinline__ Item get(int it) const {
-    const int li = it - begin;
-    return li < cap ? item_from<TILE>(s[2 * li], s[2 * li + 1]) : load_item<TILE>(g, it);
-  }
-};
-
-// Copies items [begin, min(end, begin + cap)) into shared memory (all
-// threads of the CTA take part; a __syncthreads must follow).
-__device__ __forceinline__ ItemTable stage_items(int4* dst, const int32_t* items, int begin, int end,
-                                                 int cap, int tid, int nthreads) {
-  const int n = min(end - begin, cap) * 2;
-  const int4* src = reinterpret_cast<const int4*>(items + (int64_t)begin * kItemWords);
-  for (int k = tid; k < n; k += nthreads) dst[k] = src[k];
-  return ItemTable{dst, items, begin, cap};
-}
-
 // Output epilogue of one element (index = q_head * Dv + dim into shift / smooth).
 __device__ __forceinline__ float ep_value(const OutEpilogue& e, float v, int idx) {
   if (e.shift != nullptr) v += __bfloat162float(e.shift[idx]);
@@ -121,20 +74,6 @@ __device__ __forceinline__ float ep_value(const OutEpilogue& e, float v, int idx
 __device__ __forceinline__ uint32_t ep_int8(const OutEpilogue& e, float v) {
   const float q = fminf(fmaxf(rintf(v * e.q_scale), e.q_min), e.q_max);
   return (uint32_t)(int32_t)q & 0xFFu;
-}
-
-// One output element through the epilogue into out (bf16 or int8), out of
-// line so that kernels carry a single copy of it.
-static __device__ PA_COLD void ep_store1(const OutEpilogue e, void* out, int64_t o, int idx, float v) {
-  v = ep_value(e, v, idx);
-  if (e.int8_out)
-    reinterpret_cast<int8_t*>(out)[o] = (int8_t)ep_int8(e, v);
-  else
-    reinterpret_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(v);
-}
-
-__device__ __forceinline__ bool ep_active(const OutEpilogue& e) {
-  return e.shift != nullptr || e.smooth != nullptr || e.int8_out != 0;
 }
 
 // Final output of 16 consecutive dims (idx0 = q_head * Dv + first dim) to out
@@ -169,7 +108,7 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
 // %globaltimer stamp of pipeline event `ev` of tile g (diagnostic trace)
 // The stamp itself is out of line: a traced call site costs the hot loops a
 // compare and a branch.
-static __device__ PA_COLD void trace_rec(uint64_t* trace, int ctas, int tiles, uint32_t g, int ev) {
+static __device__ __noinline__ void trace_rec(uint64_t* trace, int ctas, int tiles, uint32_t g, int ev) {
   if ((int)blockIdx.x < ctas && (int)g < tiles)
     trace[((int64_t)blockIdx.x * tiles + g) * 16 + ev] = globaltimer();
 }

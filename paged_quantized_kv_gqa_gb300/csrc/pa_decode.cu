@@ -17,7 +17,9 @@
 //                 position): running max (lazy, vote per half), row sums in
 //                 registers, P^T to shared memory, the rare rescale of its
 //                 columns of O, and the epilogue of its rows (one tile after
-//                 the item's last PV was queued);
+//                 the item's last PV was queued).  When every item's rows fit
+//                 in the first half (e.g. one token of a group of 4), SM1 has
+//                 only padding rows and leaves at once;
 //       CV        Q' of each item, K rows (lane = position) and V^T rows (lane
 //                 = head dim) dequantised straight into TMEM;
 //       IO        one TMA warp ((page, kv head) K slab [64 x 128] with 128B
@@ -172,11 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 2; ++j) {
       mbar_init(&kready[j], 4);
       mbar_init(&sfull[j], 1);
-      mbar_init(&sfree[j], 8);
+      mbar_init(&sfree[j], 4 * p.softmax_wgs);
       mbar_init(&vready[j], 4);
     }
     for (int j = 0; j < kPBufs; ++j) {
-      mbar_init(&pready[j], 8);
+      mbar_init(&pready[j], 4 * p.softmax_wgs);
       mbar_init(&pvdone[j], 1);
     }
     *abort_any = 0;
@@ -330,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int li = it - item_begin;
         const uint64_t t0 = globaltimer();
         while (true) {
-          const bool done = lane >= 8 || ep_done[lane] > li;
+          const bool done = lane >= 4 * p.softmax_wgs || ep_done[lane] > li;
           if (__all_sync(0xffffffffu, done)) break;
           const bool give_up = *abort_any || globaltimer() - t0 > limit;
           if (__shfl_sync(0xffffffffu, give_up, 0)) { ok = false; break; }
@@ -378,6 +380,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_any = 1;
       }
     }
+  } else if (wg == 1 && p.softmax_wgs == 1) {
+    // every item's rows are in the first half: this warpgroup has no rows
   } else if (wg < 2) {
     // ================================================================ softmax
     // warpgroup wg owns packed rows [r_lo, r_lo + NH); lane = position

@@ -112,6 +112,7 @@ struct AttnParams {
   int32_t max_chunks;
   int32_t skip_first_load;
   int32_t q_box_tokens;  // query tokens per TMA box of the item's Q rows (append)
+  int32_t softmax_wgs;   // decode: softmax warpgroups in use (1 when every item's rows fit in half)
   float sm_scale_log2;   // sm_scale * log2(e)
   OutEpilogue ep;
   const int32_t* cu_seqlens_q;   // device, needed with a tree mask
