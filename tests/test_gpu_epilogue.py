@@ -65,6 +65,9 @@ def _run(case, int8_out, in_scale=0.5):
 CASES = [
     ("decode", dict(seq_lens=[1, 1, 6], seq_lens_kv=[40, 700, 300], q_heads=32, kv_heads=8,
                     chunk_size=256)),
+    # one token per sequence, group of 4: the decode kernel's epilogue warpgroup writes the rows
+    ("decode", dict(seq_lens=[1, 1, 1], seq_lens_kv=[40, 700, 300], q_heads=32, kv_heads=8,
+                    chunk_size=256)),
     ("append", dict(seq_lens=[70, 130], seq_lens_kv=[30, 600], q_heads=32, kv_heads=8,
                     chunk_size=256)),
     ("append", dict(seq_lens=[90], seq_lens_kv=[100], q_heads=16, kv_heads=4,
