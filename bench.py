@@ -53,16 +53,17 @@ def _peaks(bound: str):
 # `ncu --set full` capture (summaries under profiles/).  A figure is reported
 # only while the kernel source still hashes to the version it was taken with.
 NCU_TRAFFIC = {
-    "decode-2": ("pa_decode.cu", "f5eb6755bf6df5db", 319.333632e6 + 5.314560e6),
-    "append-3": ("pa_append.cu", "d3108ca4e473eb65", 72.359168e6 + 3.082240e6),
-    "mla-5": ("pa_mla.cu", "61e949fe9751d07a", 199.316224e6 + 23.848960e6),
+    "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "b89cf2e7c1a69a26", 319.353088e6 + 5.194240e6),
+    "append-3": (("pa_append.cu",), "63582a2813566750", 72.314368e6 + 2.772224e6),
+    "mla-5": (("pa_mla.cu",), "42a7f6c4f0970e85", 199.362560e6 + 23.201024e6),
 }
 
 
-def _kernel_sha(fname: str) -> str:
+def _kernel_sha(files) -> str:
+    """Hash of a kernel's source files and the headers every kernel includes."""
     import hashlib
     h = hashlib.sha256()
-    for n in (fname, "pa_common.cuh", "pa_ptx.cuh"):
+    for n in tuple(files) + ("pa_common.cuh", "pa_ptx.cuh", "pa_internal.h"):
         with open(os.path.join(ROOT, "paged_quantized_kv_gqa_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -70,7 +71,7 @@ def _kernel_sha(fname: str) -> str:
 
 def _traffic(workload: str):
     ent = NCU_TRAFFIC.get(workload)
-    if ent is None or _kernel_sha(ent[0]) != ent[1]:
+    if ent is None or ent[1] is None or _kernel_sha(ent[0]) != ent[1]:
         return None
     return int(ent[2])
 

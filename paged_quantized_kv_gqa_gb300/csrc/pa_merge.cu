@@ -13,8 +13,10 @@
 
 namespace pa {
 
+// 512-wide rows: five blocks per SM, so that a 128-head MLA batch's rows are
+// merged in one wave
 template <int DV>
-__global__ void __launch_bounds__(256) merge_kernel(const int32_t* __restrict__ merge_tokens,
+__global__ void __launch_bounds__(256, DV >= 512 ? 5 : 1) merge_kernel(const int32_t* __restrict__ merge_tokens,
                                                     const int32_t* __restrict__ nch_token,
                                                     int n_merge, int q_heads, int max_chunks,
                                                     const __nv_bfloat16* __restrict__ part_o,

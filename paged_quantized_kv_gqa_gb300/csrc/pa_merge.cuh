@@ -17,9 +17,10 @@ namespace pa {
 
 // Merges R rows with one warp (all lanes call it; rows with valid[r] false
 // come out with W = 0).  The partial states are read through L2 only (other
-// CTAs of the same launch may have written them).  Lane l owns output elements [l * DV / 32, + DV / 32);
-// lane c holds the weight of chunk c0 + c, and each row's chunk vectors are
-// read four chunks at a time so that their loads are in flight together.
+// CTAs of the same launch may have written them).  Lane l owns output elements
+// [l * DV / 32, + DV / 32); lane c holds the weight of chunk c0 + c, and each
+// row's chunk vectors are read several chunks at a time so that their loads
+// are in flight together.
 template <int DV, int R>
 __device__ __forceinline__ void merge_rows(const __nv_bfloat16* __restrict__ part_o,
                                            const float* __restrict__ part_m,
@@ -29,6 +30,12 @@ __device__ __forceinline__ void merge_rows(const __nv_bfloat16* __restrict__ par
                                            float (&acc)[R][DV / 32], float (&M)[R], float (&W)[R]) {
   constexpr int kPer = DV / 32;
   static_assert(kPer % 4 == 0, "lane slice must be a multiple of 4 elements");
+  // a lane reads its slice of a chunk row as 16-byte vectors where it can (8
+  // bf16), else 8-byte ones; kU chunk rows are in flight per pass (fewer for
+  // wide rows, to keep the registers and hence the occupancy up)
+  constexpr int kVecBytes = (kPer % 8 == 0) ? 16 : 8;
+  constexpr int kVec = kPer * 2 / kVecBytes;
+  constexpr int kU = DV >= 512 ? 1 : 4;
   float m0[R], d0[R];   // chunk `lane` of each row (the first pass of 32)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
@@ -69,35 +76,44 @@ __device__ __forceinline__ void merge_rows(const __nv_bfloat16* __restrict__ par
       W[r] += w[r];
     }
     const int n = min(32, nch - c0);
-    for (int j = 0; j < n; j += 4) {
-      float wj[R][4];
-      uint2 raw[R][4][kPer / 4];
+    for (int j = 0; j < n; j += kU) {
+      float wj[R][kU];
+      uint4 raw[R][kU][kVec];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kU; ++u) {
           wj[r][u] = __shfl_sync(0xffffffffu, w[r], (j + u) & 31);
           const __nv_bfloat16* src =
               part_o + (slot0[r] + (c0 + j + u) * cstride) * DV + lane * kPer;
 #pragma unroll
-          for (int k = 0; k < kPer / 4; ++k)
-            raw[r][u][k] = (j + u < n && wj[r][u] != 0.f)
-                               ? __ldcg(reinterpret_cast<const uint2*>(src + 4 * k))
-                               : make_uint2(0u, 0u);
+          for (int k = 0; k < kVec; ++k) {
+            raw[r][u][k] = make_uint4(0u, 0u, 0u, 0u);
+            if (j + u < n && wj[r][u] != 0.f) {
+              if constexpr (kVecBytes == 16) {
+                raw[r][u][k] = __ldcg(reinterpret_cast<const uint4*>(src) + k);
+              } else {
+                const uint2 h = __ldcg(reinterpret_cast<const uint2*>(src) + k);
+                raw[r][u][k].x = h.x;
+                raw[r][u][k].y = h.y;
+              }
+            }
+          }
         }
       }
 #pragma unroll
       for (int r = 0; r < R; ++r) {
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kU; ++u) {
 #pragma unroll
-          for (int k = 0; k < kPer / 4; ++k) {
-            const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&raw[r][u][k].x);
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&raw[r][u][k].y);
-            acc[r][4 * k + 0] += wj[r][u] * __low2float(a);
-            acc[r][4 * k + 1] += wj[r][u] * __high2float(a);
-            acc[r][4 * k + 2] += wj[r][u] * __low2float(b);
-            acc[r][4 * k + 3] += wj[r][u] * __high2float(b);
+          for (int k = 0; k < kVec; ++k) {
+            const uint32_t wd[4] = {raw[r][u][k].x, raw[r][u][k].y, raw[r][u][k].z, raw[r][u][k].w};
+#pragma unroll
+            for (int e = 0; e < kVecBytes / 4; ++e) {
+              const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&wd[e]);
+              acc[r][k * (kVecBytes / 2) + 2 * e + 0] += wj[r][u] * __low2float(b2);
+              acc[r][k * (kVecBytes / 2) + 2 * e + 1] += wj[r][u] * __high2float(b2);
+            }
           }
         }
       }
