@@ -53,9 +53,9 @@ def _peaks(bound: str):
 # `ncu --set full` capture (summaries under profiles/).  A figure is reported
 # only while the kernel source still hashes to the version it was taken with.
 NCU_TRAFFIC = {
-    "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "b89cf2e7c1a69a26", 319.353088e6 + 5.194240e6),
-    "append-3": (("pa_append.cu",), "63582a2813566750", 72.314368e6 + 2.772224e6),
-    "mla-5": (("pa_mla.cu",), "42a7f6c4f0970e85", 199.362560e6 + 23.201024e6),
+    "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "5a4d8e6ffaaad61b", 319.336448e6 + 4.516096e6),
+    "append-3": (("pa_append.cu",), "9ef2b9da1e81654a", 72.312064e6 + 2.669056e6),
+    "mla-5": (("pa_mla.cu",), "c4d1e50f724ae84a", 199.299072e6 + 22.765824e6),
 }
 
 

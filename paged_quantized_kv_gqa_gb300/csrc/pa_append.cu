@@ -609,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_launch_dependents();   // the merge grid may be scheduled while the last CTAs finish
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 

@@ -25,6 +25,7 @@ __global__ void __launch_bounds__(256, DV >= 512 ? 5 : 1) merge_kernel(const int
                                                     void* __restrict__ out,
                                                     float* __restrict__ lse,
                                                     const OutEpilogue ep) {
+  pdl_wait();   // launched as a programmatic dependent of the attention kernel
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (wid >= n_merge * q_heads) return;
@@ -44,18 +45,29 @@ cudaError_t launch_merge(const Plan& plan, const WsView& ws, void* out, float* l
   if (n_merge == 0) return cudaSuccess;
   const int warps = n_merge * plan.prob.q_heads;
   const int blocks = (warps + 7) / 8;
-  if (plan.prob.head_dim_v == 128) {
-    merge_kernel<128><<<blocks, 256, 0, stream>>>(ws.merge_tokens, ws.nch_token, n_merge,
-                                                 plan.prob.q_heads, plan.max_chunks, ws.part_o,
-                                                 ws.part_m, ws.part_d, out, lse, ep);
-  } else if (plan.prob.head_dim_v == 512) {
-    merge_kernel<512><<<blocks, 256, 0, stream>>>(ws.merge_tokens, ws.nch_token, n_merge,
-                                                 plan.prob.q_heads, plan.max_chunks, ws.part_o,
-                                                 ws.part_m, ws.part_d, out, lse, ep);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  // programmatic dependent launch: the grid is set up while the attention
+  // kernel's last CTAs finish, and waits for it in pdl_wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int32_t* mt = ws.merge_tokens;
+  const int32_t* nt = ws.nch_token;
+  const int qh = plan.prob.q_heads, mc = plan.max_chunks;
+  const __nv_bfloat16* po = ws.part_o;
+  const float* pm = ws.part_m;
+  const float* pd = ws.part_d;
+  if (plan.prob.head_dim_v == 128)
+    return cudaLaunchKernelEx(&cfg, merge_kernel<128>, mt, nt, n_merge, qh, mc, po, pm, pd, out, lse, ep);
+  if (plan.prob.head_dim_v == 512)
+    return cudaLaunchKernelEx(&cfg, merge_kernel<512>, mt, nt, n_merge, qh, mc, po, pm, pd, out, lse, ep);
+  return cudaErrorInvalidValue;
 }
 
 // ------------------------------------------------------------------ gather

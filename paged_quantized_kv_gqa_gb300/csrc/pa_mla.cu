@@ -596,6 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
   cluster_sync();   // no CTA leaves while its peer may still touch its shared memory
+  pdl_launch_dependents();   // the merge grid may be scheduled while the last CTAs finish
 }
 
 template <int FP8>
