@@ -50,8 +50,9 @@ def _peaks(bound: str):
 
 
 # DRAM bytes (read + written) per launch of each attention kernel, from one
-# `ncu --set full` capture (summaries under profiles/).  A figure is reported
-# only while the kernel source still hashes to the version it was taken with.
+# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on the workload
+# (profiles/traffic_attention_kernels.md).  A figure is reported only while
+# the kernel's sources still hash to the version it was taken with.
 NCU_TRAFFIC = {
     "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "5a4d8e6ffaaad61b", 319.336448e6 + 4.516096e6),
     "append-3": (("pa_append.cu",), "9ef2b9da1e81654a", 72.312064e6 + 2.669056e6),
