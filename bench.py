@@ -33,6 +33,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "KV-cache HBM GB/s (decode) & TFLOP/s (append/MLA), % of GB300 roofline"
+L2_BYTES = 129 * 1000 * 1000          # GB300 L2 (129 MB)
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -253,30 +254,88 @@ def run_cuda(args) -> dict:
     if st != 0:
         raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
 
-    # end to end through the public API with host buffers: q / lengths / table up,
-    # plan upload, run, merge, out + lse down, all inside the timed region
+    # end to end through the public API with host buffers, as a serving loop
+    # runs it: every step uploads its inputs (q, block table, plan) from pinned
+    # host memory, runs, merges and reads its output and lse back into pinned
+    # host memory.  Two sets of device inputs / outputs / workspaces alternate,
+    # so step i+1's upload (copy stream) and step i-1's download (second copy
+    # stream) overlap step i's kernels; events order each buffer's reuse.  The
+    # timed region runs from the first upload to the last result in host
+    # memory.  L2 is not flushed in between; instead the steps rotate over enough
+    # copies of the cache that more than twice the L2 size is read between two
+    # uses of one copy (one copy when the cache alone is that large).
+    same_kv = d.get("cache_v") is None or d["cache_v"].data_ptr() == d["cache_k"].data_ptr()
+    n_rot = max(1, -(-2 * L2_BYTES // max(1, kv_bytes)))   # kv_bytes: cache bytes one step reads
+    caches = [(d["cache_k"], d["cache_v"])]
+    for _ in range(n_rot - 1):
+        ck = d["cache_k"].clone()
+        caches.append((ck, ck if same_kv else d["cache_v"].clone()))
     q_h = d["q"].cpu().pin_memory()
     bt_h = d["block_table"].cpu().pin_memory()
-    out_h = torch.empty_like(d["out"], device="cpu").pin_memory()
-    lse_h = torch.empty_like(d["lse"], device="cpu").pin_memory()
     plan_words = (desc["num_ctas"] + 1) + desc["num_items"] * 8 + desc["total_q"] + \
         len(desc["merge_tokens"])
     h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + plan_words * 4
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * 4
-    e2e_ms = []
-    for i in range(max(3, K)):
-        flush.fill_(i & 0xFF)
-        a, _, b = ev[i % K]
-        a.record(stream)
-        d["q"].copy_(q_h, non_blocking=True)
-        d["block_table"].copy_(bt_h, non_blocking=True)
-        pa.pa_plan_upload(plan, ws, stream)
-        step()
-        out_h.copy_(d["out"], non_blocking=True)
-        lse_h.copy_(d["lse"], non_blocking=True)
-        b.record(stream)
+    d2h = d["out"].numel() * d["out"].element_size() + d["lse"].numel() * 4
+    sets = []
+    for k in range(2):
+        qk = torch.empty_like(d["q"])
+        btk = torch.empty_like(d["block_table"])
+        outk = torch.empty_like(d["out"])
+        lsek = torch.empty_like(d["lse"])
+        wsk = torch.zeros(plan.workspace_size, dtype=torch.uint8, device=dev)
+        ak = [pa.make_args(q=qk, cache_k=ck, cache_v=cv, k_scale=d["k_scale"],
+                           v_scale=d["v_scale"], block_table=btk, out=outk, lse=lsek,
+                           seq_lens=d["seq_lens"], seq_lens_kv=d["seq_lens_kv"],
+                           cu_seqlens_q=d["cu_seqlens_q"], attn_mask=d.get("attn_mask"))
+              for ck, cv in caches]
+        sets.append(dict(q=qk, bt=btk, out=outk, lse=lsek, ws=wsk, args=ak,
+                         out_h=torch.empty_like(d["out"], device="cpu").pin_memory(),
+                         lse_h=torch.empty_like(d["lse"], device="cpu").pin_memory()))
+    up_s, down_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_e2e = max(8, K)
+
+    def e2e_pass():
+        ev_up = [torch.cuda.Event() for _ in range(n_e2e)]
+        ev_run = [torch.cuda.Event() for _ in range(n_e2e)]
+        ev_down = [torch.cuda.Event() for _ in range(n_e2e)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
-        e2e_ms.append(a.elapsed_time(b))
+        t0.record(up_s)
+        for i in range(n_e2e):
+            sk = sets[i & 1]
+            if i >= 2:
+                up_s.wait_event(ev_run[i - 2])      # step i-2 has read this set's inputs
+            with torch.cuda.stream(up_s):
+                sk["q"].copy_(q_h, non_blocking=True)
+                sk["bt"].copy_(bt_h, non_blocking=True)
+            pa.pa_plan_upload(plan, sk["ws"], up_s)
+            ev_up[i].record(up_s)
+            stream.wait_event(ev_up[i])
+            if i >= 2:
+                stream.wait_event(ev_down[i - 2])   # step i-2's result has left this set's out
+            ak = sk["args"][i % n_rot]
+            pa.pa_run(plan, ak, sk["ws"], stream)
+            if split:
+                pa.pa_merge(plan, ak, sk["ws"], stream)
+            ev_run[i].record(stream)
+            down_s.wait_event(ev_run[i])
+            with torch.cuda.stream(down_s):
+                sk["out_h"].copy_(sk["out"], non_blocking=True)
+                sk["lse_h"].copy_(sk["lse"], non_blocking=True)
+            ev_down[i].record(down_s)
+        up_s.wait_stream(down_s)
+        t1.record(up_s)
+        torch.cuda.synchronize(dev)
+        return t0.elapsed_time(t1) / n_e2e
+
+    e2e_pass()                                      # warm-up
+    e2e_ms = [e2e_pass() for _ in range(2)]
+    for sk in sets:                                 # every step's result is the path's result
+        st, det = pa.pa_check(plan, sk["ws"], stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+    if not torch.equal(sets[0]["out_h"].view(torch.int16), d["out"].cpu().view(torch.int16)):
+        raise RuntimeError("end-to-end output differs from the device-timed run")
     e2e = _job_rate(work, world, _max_over_ranks(statistics.mean(e2e_ms), world))
 
     res = {
@@ -296,7 +355,11 @@ def run_cuda(args) -> dict:
                      "peak_source": peak_kind, "kernel": "pa_run attention kernel",
                      "run_ms": round(run_mean, 5)},
         "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "mode": "steps back to back: each step's upload and result read overlap the "
+                        "neighbouring steps' kernels (two buffer sets, copy streams)",
+                "l2": f"not flushed; steps rotate over {n_rot} cache cop{'y' if n_rot == 1 else 'ies'} "
+                      f"({kv_bytes / 1e6:.0f} MB read per step; > 2x L2 read between reuses)"},
         "gpu_launches": K * (2 if split else 1),
         "clocks": clk.summary(),
     }
