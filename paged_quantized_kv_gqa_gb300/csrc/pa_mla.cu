@@ -362,21 +362,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int li = it - item_begin;
       if (q_loader) {
         // Q' of the item -> TMEM (thread = head row; 576 bf16 -> 288 fp16x2
-        // columns) once the S MMAs of the previous item completed
+        // columns) in six rounds of 12 16-byte loads; the first round is in
+        // flight before the S MMAs of the previous item release Q's columns
+        const uint4* src = reinterpret_cast<const uint4*>(p.q + (int64_t)m.tok0 * p.q_stride +
+                                                          (int64_t)t * kDqk);
+        uint4 r[12];
+#pragma unroll
+        for (int k = 0; k < 12; ++k) r[k] = src[k];
         if (li > 0 && !wait_or_abort(qfree, (li - 1) & 1, limit, abort_any)) {
           fail = true;
           break;
         }
         if (t == 0) trace_ev(p, g, 3);
-        const uint4* src = reinterpret_cast<const uint4*>(p.q + (int64_t)m.tok0 * p.q_stride +
-                                                          (int64_t)t * kDqk);
 #pragma unroll 1
-        for (int c0 = 0; c0 < 18; c0 += 2) {
-          uint4 r[8];
+        for (int ph = 0; ph < 6; ++ph) {
+          if (ph > 0) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) r[k] = src[4 * c0 + k];
+            for (int k = 0; k < 12; ++k) r[k] = src[12 * ph + k];
+          }
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 3; ++c) {
             uint32_t w[16];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
@@ -386,7 +391,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 w[4 * k + e] =
                     pack_half2(__bfloat162float(hv[2 * e]), __bfloat162float(hv[2 * e + 1]));
             }
-            tmem_st16(t_lane + 16 * (c0 + c), w);
+            tmem_st16(t_lane + 48 * ph + 16 * c, w);
           }
         }
         tmem_wait_st();
