@@ -55,7 +55,7 @@ def _peaks(bound: str):
 # (profiles/traffic_attention_kernels.md).  A figure is reported only while
 # the kernel's sources still hash to the version it was taken with.
 NCU_TRAFFIC = {
-    "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "5a4d8e6ffaaad61b", 319.336448e6 + 4.516096e6),
+    "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "2dba40f4d753ecc7", 319.408384e6 + 4.340224e6),
     "append-3": (("pa_append.cu",), "9ef2b9da1e81654a", 72.312064e6 + 2.669056e6),
     "mla-5": (("pa_mla.cu",), "4389a6443d093cda", 199.314688e6 + 22.971392e6),
 }

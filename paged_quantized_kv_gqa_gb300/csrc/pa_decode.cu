@@ -654,6 +654,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ CV warpgroup
     // Q' of each item, K rows (lane = position) and V^T rows (lane = head dim)
     // into TMEM
+    // This warpgroup runs ahead of the softmax, so its waits suspend for the
+    // hardware's default time rather than re-probing every 32 ns (fewer issue
+    // slots taken from the softmax warps on the same sub-partitions).
     const int d = tid & 127;  // TMEM lane: K position / V head dim / output dim
     uint32_t g = 0;
     bool fail = false;
@@ -702,12 +705,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int stage = g % kStages;
         // K buffer g&1 was last read by S_{g-2}; Q' buffer li&1 by the S of item
         // li-2, whose last tile is at most g-2
-        if (g >= 2 && !dwait(&sfull[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
+        if (g >= 2 && !wait_or_abort(&sfull[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
           note_fail(it);
           break;
         }
         if (i == 0) load_q(m, q_s + (li & 1) * NR * 256);
-        if (!dwait(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
+        if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
         if (d == 0) trace_ev(p, g, 1);
         {
           const int box = d >> 6, row = d & 63;
@@ -735,7 +738,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_arrive(&kready[g & 1], lane);
         if (d == 0) trace_ev(p, g, 2);
         // V buffer g&1 was last read by PV_{g-2}
-        if (g >= 2 && !dwait(&pvdone[(g - 2) & 3], ((g - 2) >> 2) & 1, limit, abort_any)) {
+        if (g >= 2 && !wait_or_abort(&pvdone[(g - 2) & 3], ((g - 2) >> 2) & 1, limit, abort_any)) {
           note_fail(it);
           break;
         }
