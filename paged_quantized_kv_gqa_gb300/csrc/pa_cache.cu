@@ -10,10 +10,12 @@
 // its scale, then int8 round-half-even saturated to +-127, or E4M3
 // round-to-nearest-even saturated to +-448.
 //
-// One CTA per (sequence, page of the appended range, kv head), thread = head
-// dim: reads of the new rows and writes of K rows are coalesced, each thread
-// writes its own V^T row segment (16 bytes at a time), and the loads of 16
-// positions are issued before their stores.
+// One CTA per (sequence, page of the appended range, kv head).  When the new
+// rows are 16-byte aligned (GQA), each thread reads 8 dims of a position per
+// 16-byte load (all of a page's loads in flight at once), writes 8-byte K row
+// pieces, and V goes through shared memory so that thread = dim writes its V^T
+// row 16 bytes at a time.  Otherwise (and for MLA rows) thread = dim with
+// 2-byte reads, 16 positions' loads in flight before their stores.
 #include "pa_common.cuh"
 
 namespace pa {
@@ -56,7 +58,7 @@ struct AppendParams {
   int32_t mla;
 };
 
-template <int FP8>
+template <int FP8, bool VEC>
 __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendParams p) {
   const int b = blockIdx.x;
   const int kvh = blockIdx.z;
@@ -105,12 +107,73 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
     }
     return;
   }
+  const int64_t slab = (int64_t)page * p.kv_heads + kvh;
+  if constexpr (VEC) {
+    // 16-byte rows in and out: thread t reads dims 8 (t & 15) .. + 7 of
+    // positions (t >> 4) + 8 k, writes those 8 K bytes into the K row, and
+    // stages the 8 V bytes in shared memory [position][dim]; then thread = dim
+    // gathers its V^T row segment and writes it 16 bytes at a time
+    __shared__ __align__(16) uint8_t vs[kPage][128];
+    const int c8 = threadIdx.x & 15, r8 = threadIdx.x >> 4;
+    const int n = p1 - p0;
+    float sk[8], sv[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const int idx = p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * 128 + 8 * c8 + e : kvh;
+      sk[e] = load_scale(p.k_scale, p.scale_kind, idx);
+      sv[e] = load_scale(p.v_scale, p.scale_kind, idx);
+    }
+    uint8_t* kpage = p.cache_k + slab * kPage * 128;
+    uint4 rk[8], rv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int pos = r8 + 8 * k;
+      if (pos < n) {
+        const int64_t src = (int64_t)(t0 + pos) * p.kv_stride + (int64_t)kvh * 128 + 8 * c8;
+        rk[k] = *reinterpret_cast<const uint4*>(p.k_new + src);
+        rv[k] = *reinterpret_cast<const uint4*>(p.v_new + src);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int pos = r8 + 8 * k;
+      if (pos < n) {
+        const int off = (p0 + pos) % kPage;
+        const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(&rk[k]);
+        const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&rv[k]);
+        uint32_t wk[2] = {0, 0}, wv[2] = {0, 0};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          wk[e >> 2] |= (uint32_t)quantize<FP8>(__bfloat162float(hk[e]), sk[e]) << (8 * (e & 3));
+          wv[e >> 2] |= (uint32_t)quantize<FP8>(__bfloat162float(hv[e]), sv[e]) << (8 * (e & 3));
+        }
+        *reinterpret_cast<uint2*>(kpage + off * 128 + 8 * c8) = make_uint2(wk[0], wk[1]);
+        *reinterpret_cast<uint2*>(&vs[off][8 * c8]) = make_uint2(wv[0], wv[1]);
+      }
+    }
+    __syncthreads();
+    const int d = threadIdx.x;
+    uint8_t* vrow = p.cache_v + (slab * 128 + d) * kPage;
+    const int a = p0 % kPage, e_end = a + n;
+    for (int base = a; base < e_end;) {
+      const int next = min(e_end, (base / 16 + 1) * 16);
+      if (next - base == 16) {
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) w[j >> 2] |= (uint32_t)vs[base + j][d] << (8 * (j & 3));
+        *reinterpret_cast<uint4*>(vrow + base) = make_uint4(w[0], w[1], w[2], w[3]);
+      } else {
+        for (int j = base; j < next; ++j) vrow[j] = vs[j][d];
+      }
+      base = next;
+    }
+    return;
+  }
   const int d = threadIdx.x;   // head dim (GQA head_dim 128)
   const float sk = load_scale(p.k_scale, p.scale_kind,
                               p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * 128 + d : kvh);
   const float sv = load_scale(p.v_scale, p.scale_kind,
                               p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * 128 + d : kvh);
-  const int64_t slab = (int64_t)page * p.kv_heads + kvh;
   uint8_t* krow = p.cache_k + slab * kPage * 128;
   uint8_t* vrow = p.cache_v + (slab * 128 + d) * kPage;
   const __nv_bfloat16* kin = p.k_new + (int64_t)kvh * 128 + d;
@@ -175,10 +238,16 @@ cudaError_t launch_cache_append(const Plan& plan, const pa_args& a, const void* 
   // pages an appended range of max_q positions can touch
   const int npg = (plan.max_q + kPage - 1) / kPage + 1;
   const dim3 grid(pr.bsz, npg, p.mla ? 1 : pr.kv_heads);
-  if (pr.kv_dtype == PA_KV_FP8_E4M3)
-    cache_append_kernel<1><<<grid, kThreads, 0, stream>>>(p);
-  else
-    cache_append_kernel<0><<<grid, kThreads, 0, stream>>>(p);
+  // 16-byte row access when the new rows allow it (GQA only)
+  const bool vec = !p.mla && kv_stride % 8 == 0 && reinterpret_cast<uintptr_t>(k_new) % 16 == 0 &&
+                   reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
+  if (pr.kv_dtype == PA_KV_FP8_E4M3) {
+    if (vec) cache_append_kernel<1, true><<<grid, kThreads, 0, stream>>>(p);
+    else cache_append_kernel<1, false><<<grid, kThreads, 0, stream>>>(p);
+  } else {
+    if (vec) cache_append_kernel<0, true><<<grid, kThreads, 0, stream>>>(p);
+    else cache_append_kernel<0, false><<<grid, kThreads, 0, stream>>>(p);
+  }
   return cudaGetLastError();
 }
 

@@ -15,7 +15,7 @@ from gpu_helpers import num_sms, compare
 pytestmark = pytest.mark.gpu
 
 
-def _append_on_gpu(case, packed=False):
+def _append_on_gpu(case, packed=False, misaligned=False):
     import paged_quantized_kv_gqa_gb300 as pa
     d = to_device(case, generate_on_device=False)
     k, v = new_kv(case)
@@ -32,6 +32,15 @@ def _append_on_gpu(case, packed=False):
         qkv[:, (Hq + Hkv) * D:] = torch.from_numpy(
             v.reshape(T, -1).view(np.int16)).view(torch.bfloat16).cuda()
         k_dev, v_dev, stride = qkv[:, Hq * D:], qkv[:, (Hq + Hkv) * D:], (Hq + 2 * Hkv) * D
+    elif misaligned:
+        # rows that start 2 bytes past a 16-byte boundary: the kernel's 2-byte path
+        stride = case.kv_heads * case.head_dim_qk + 1
+        kb = torch.zeros(T * stride + 1, dtype=torch.bfloat16, device="cuda")
+        vb = torch.zeros(T * stride + 1, dtype=torch.bfloat16, device="cuda")
+        k_dev = kb[1:].view(T, stride)
+        v_dev = vb[1:].view(T, stride)
+        k_dev[:, :stride - 1] = torch.from_numpy(k.reshape(T, -1).view(np.int16)).view(torch.bfloat16).cuda()
+        v_dev[:, :stride - 1] = torch.from_numpy(v.reshape(T, -1).view(np.int16)).view(torch.bfloat16).cuda()
     else:
         k_dev = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).cuda()
         v_dev = torch.from_numpy(v.view(np.int16)).view(torch.bfloat16).cuda()
@@ -74,6 +83,14 @@ def test_cache_append_from_packed_qkv():
     case = synth.make_case(name="append-qkv", seed=18, seq_lens=[50, 20], seq_lens_kv=[10, 200],
                            q_heads=16, kv_heads=4)
     ck, cv, rk, rv, *_ = _append_on_gpu(case, packed=True)
+    assert np.array_equal(ck, rk) and np.array_equal(cv, rv)
+
+
+def test_cache_append_misaligned_rows():
+    """New rows that are only 2-byte aligned take the kernel's 2-byte path."""
+    case = synth.make_case(name="append-mis", seed=20, seq_lens=[45, 70], seq_lens_kv=[19, 128],
+                           q_heads=16, kv_heads=4, scale_kind="per_channel")
+    ck, cv, rk, rv, *_ = _append_on_gpu(case, misaligned=True)
     assert np.array_equal(ck, rk) and np.array_equal(cv, rv)
 
 
