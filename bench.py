@@ -56,6 +56,11 @@ def _peaks(bound: str):
 # the kernel's sources still hash to the version it was taken with.
 NCU_TRAFFIC = {
     "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "2dba40f4d753ecc7", 319.408384e6 + 4.340224e6),
+    # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
+    # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
+    # states written both grow per sequence
+    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "2dba40f4d753ecc7",
+                      (729.514752e6 + 31.732480e6) * 7.492152264116904),
     "append-3": (("pa_append.cu",), "9ef2b9da1e81654a", 72.312064e6 + 2.669056e6),
     "mla-5": (("pa_mla.cu",), "4389a6443d093cda", 199.314688e6 + 22.971392e6),
 }
@@ -170,10 +175,9 @@ class Clocks:
                 "samples": len(rows)}
 
 
-def _workload(config: int):
+def _workload(config: int, bsz: int = 0):
     import synth
-    case = synth.config(config)
-    return case
+    return synth.config(config, bsz)
 
 
 def run_cuda(args) -> dict:
@@ -184,7 +188,7 @@ def run_cuda(args) -> dict:
     rank, world, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = _workload(args.config)
+    case = _workload(args.config, args.bsz)
     if args.tree_mask:
         from synth.cases import tree_mask
         case.attn_mask = tree_mask(case)
@@ -552,6 +556,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tree-mask", action="store_true",
                     help="speculative verify with a seeded draft-tree mask (decode-family workloads)")
+    ap.add_argument("--bsz", type=int, default=0,
+                    help="keep only the first BSZ sequences of the workload (same draws): a smaller "
+                         "case of the same kernel for profiling captures; not a bench line")
     ap.add_argument("--fused-merge", action="store_true",
                     help="decode-family workloads: merge split rows inside the attention launch "
                          "(opt-in single-launch mode) instead of the separate merge kernel")

@@ -341,15 +341,30 @@ CONFIG_NAMES = {
 }
 
 
-def config(n: int) -> Case:
+def config(n: int, bsz_limit: int = 0) -> Case:
+    """Workload n; bsz_limit > 0 keeps only its first bsz_limit sequences (the
+    same draws), for profiling captures of workloads too large to capture."""
+    case = _config(n)
+    if bsz_limit <= 0 or bsz_limit >= case.bsz:
+        return case
+    if n not in (2, 4, 5):
+        raise ValueError("bsz_limit applies to the decode-family and MLA workloads")
+    return _config(n, bsz_limit)
+
+
+def _config(n: int, bsz_limit: int = 0) -> Case:
+    def cut(name, lens_q, lens_kv):
+        if not bsz_limit:
+            return name, lens_q, lens_kv
+        return f"{name} (first {bsz_limit} sequences)", lens_q[:bsz_limit], lens_kv[:bsz_limit]
     if n == 1:
         return make_case(name="decode-1", seed=1, seq_lens=[1, 1], seq_lens_kv=[100, 37],
                          q_heads=4, kv_heads=1, kv_dtype=INT8, scale_kind=PER_HEAD,
                          causal=True, chunk_size=0, num_pages=8, table="reshape")
     if n == 2:
         bsz = 64
-        return make_case(name="decode-2", seed=2, seq_lens=np.ones(bsz, np.int32),
-                         seq_lens_kv=_draw_lens(2, S_LEN_KV, bsz, 512, 4096),
+        name, ql, kv = cut("decode-2", np.ones(bsz, np.int32), _draw_lens(2, S_LEN_KV, bsz, 512, 4096))
+        return make_case(name=name, seed=2, seq_lens=ql, seq_lens_kv=kv,
                          q_heads=32, kv_heads=8, kv_dtype=INT8, scale_kind=PER_CHANNEL,
                          causal=True, chunk_size=512, num_pages=4096)
     if n == 3:
@@ -361,14 +376,16 @@ def config(n: int) -> Case:
                          causal=True, chunk_size=0)
     if n == 4:
         bsz = 128
-        return make_case(name="spec-verify-4", seed=4, seq_lens=np.full(bsz, 6, np.int32),
-                         seq_lens_kv=_draw_lens(4, S_LEN_KV, bsz, 8192, 32768),
+        name, ql, kv = cut("spec-verify-4", np.full(bsz, 6, np.int32),
+                           _draw_lens(4, S_LEN_KV, bsz, 8192, 32768))
+        return make_case(name=name, seed=4, seq_lens=ql, seq_lens_kv=kv,
                          q_heads=64, kv_heads=8, kv_dtype=INT8, scale_kind=PER_HEAD,
                          causal=True, chunk_size=1024)
     if n == 5:
         bsz = 32
-        return make_case(name="mla-5", seed=5, seq_lens=_draw_lens(5, S_LEN_Q, bsz, 1, 2),
-                         seq_lens_kv=_draw_lens(5, S_LEN_KV, bsz, 4096, 16384),
+        name, ql, kv = cut("mla-5", _draw_lens(5, S_LEN_Q, bsz, 1, 2),
+                           _draw_lens(5, S_LEN_KV, bsz, 4096, 16384))
+        return make_case(name=name, seed=5, seq_lens=ql, seq_lens_kv=kv,
                          q_heads=128, kv_heads=1, head_dim_qk=576, head_dim_v=512,
                          kv_dtype=FP8, scale_kind=GLOBAL, layout=MLA, causal=True,
                          chunk_size=-1, sm_scale=1.0 / math.sqrt(192.0))
