@@ -13,6 +13,70 @@
 
 namespace pa {
 
+// One row whose chunk count is at most kPre: the (m, d) loads and every chunk
+// row's loads go out in a single round (the row loads do not depend on the
+// weights), so the row costs one memory round trip instead of three.
+template <int DV, int kPre>
+__device__ __forceinline__ void merge_row_short(const __nv_bfloat16* __restrict__ part_o,
+                                                const float* __restrict__ part_m,
+                                                const float* __restrict__ part_d, int64_t slot0,
+                                                int64_t cstride, int nch, int lane,
+                                                float (&acc)[DV / 32], float& M, float& W) {
+  constexpr int kPer = DV / 32;
+  constexpr int kVecBytes = (kPer % 8 == 0) ? 16 : 8;
+  constexpr int kVec = kPer * 2 / kVecBytes;
+  float mc = -INFINITY, dc = 0.f;
+  if (lane < nch) {
+    mc = __ldcg(part_m + slot0 + lane * cstride);
+    dc = __ldcg(part_d + slot0 + lane * cstride);
+  }
+  uint4 raw[kPre][kVec];
+#pragma unroll
+  for (int c = 0; c < kPre; ++c) {
+    const __nv_bfloat16* src = part_o + (slot0 + c * cstride) * DV + lane * kPer;
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      raw[c][k] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < nch) {
+        if constexpr (kVecBytes == 16) {
+          raw[c][k] = __ldcg(reinterpret_cast<const uint4*>(src) + k);
+        } else {
+          const uint2 h = __ldcg(reinterpret_cast<const uint2*>(src) + k);
+          raw[c][k].x = h.x;
+          raw[c][k].y = h.y;
+        }
+      }
+    }
+  }
+  M = mc;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  W = 0.f;
+  if (M == -INFINITY) return;
+  const float w = (mc != -INFINITY) ? dc * __expf(mc - M) : 0.f;
+  W = w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+#pragma unroll
+  for (int c = 0; c < kPre; ++c) {
+    const float wc = __shfl_sync(0xffffffffu, w, c);
+    if (c < nch && wc != 0.f) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        const uint32_t wd[4] = {raw[c][k].x, raw[c][k].y, raw[c][k].z, raw[c][k].w};
+#pragma unroll
+        for (int e = 0; e < kVecBytes / 4; ++e) {
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&wd[e]);
+          acc[k * (kVecBytes / 2) + 2 * e + 0] += wc * __low2float(b2);
+          acc[k * (kVecBytes / 2) + 2 * e + 1] += wc * __high2float(b2);
+        }
+      }
+    }
+  }
+}
+
 // 512-wide rows: five blocks per SM, so that a 128-head MLA batch's rows are
 // merged in one wave
 template <int DV>
@@ -33,9 +97,20 @@ __global__ void __launch_bounds__(256, DV >= 512 ? 5 : 1) merge_kernel(const int
   const int head = wid % q_heads;
   const int nch = nch_token[token];
   const int64_t slot0[1] = {(int64_t)token * max_chunks * q_heads + head};
-  const bool valid[1] = {true};
   float acc[1][DV / 32], M[1], W[1];
-  merge_rows<DV, 1>(part_o, part_m, part_d, slot0, valid, q_heads, nch, lane, acc, M, W);
+  // 128-wide rows with at most 8 chunks: one round of loads (512-wide rows keep
+  // the register budget that gives five blocks per SM)
+  bool done = false;
+  if constexpr (DV < 512) {
+    if (nch <= 8) {
+      merge_row_short<DV, 8>(part_o, part_m, part_d, slot0[0], q_heads, nch, lane, acc[0], M[0], W[0]);
+      done = true;
+    }
+  }
+  if (!done) {
+    const bool valid[1] = {true};
+    merge_rows<DV, 1>(part_o, part_m, part_d, slot0, valid, q_heads, nch, lane, acc, M, W);
+  }
   merge_store<DV>(acc[0], M[0], W[0], out, lse, ep, token, head, q_heads, lane);
 }
 
