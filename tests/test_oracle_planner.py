@@ -112,3 +112,13 @@ def test_auto_chunk_rule():
     big = synth.make_case(seq_lens=[1], seq_lens_kv=[100], q_heads=4, kv_heads=1,
                           chunk_size=-1)
     assert op.plan(big, 152)["chunk"] == 0      # 256 >= 101: no split
+
+
+def test_workload_truncation_keeps_the_same_draws():
+    """A profiling capture's smaller case is the first sequences of the workload:
+    the same lengths, hence the same per-sequence cache bytes."""
+    full, part = synth.config(4), synth.config(4, 16)
+    assert part.bsz == 16 and part.name.startswith("spec-verify-4")
+    assert list(part.seq_lens) == list(full.seq_lens[:16])
+    assert list(part.seq_lens_kv) == list(full.seq_lens_kv[:16])
+    assert synth.config(2, 0).bsz == synth.config(2).bsz
