@@ -495,11 +495,22 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   if (plan->family == PA_FAMILY_DECODE) {
     CUtensorMap tk, tv;
     const uint64_t heads_total = (uint64_t)pr.num_pages * pr.kv_heads;
-    s = make_map(&tk, args->cache_k, heads_total * 64, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (s != PA_OK) return s;
-    s = make_map(&tv, args->cache_v, heads_total * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
-    if (s != PA_OK) return s;
-    e = launch_decode(*plan, p, tk, tv, st);
+    if (plan->max_q * p.group <= kWarpDecodeRows && !plan->fused_merge) {
+      // up to 16 packed rows: one warp per item with the tile in registers,
+      // half a page per copy (K [32 x 128] 128B-swizzled, V^T [128 x 32])
+      s = make_map(&tk, args->cache_k, heads_total * 64, 128, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (s != PA_OK) return s;
+      s = make_map(&tv, args->cache_v, heads_total * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_NONE, 32);
+      if (s != PA_OK) return s;
+      e = launch_decode_warp(*plan, p, tk, tv, st);
+    } else {
+      // more rows (or the in-kernel merge): the tensor-memory kernel
+      s = make_map(&tk, args->cache_k, heads_total * 64, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+      if (s != PA_OK) return s;
+      s = make_map(&tv, args->cache_v, heads_total * 128, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B);
+      if (s != PA_OK) return s;
+      e = launch_decode(*plan, p, tk, tv, st);
+    }
   } else if (plan->family == PA_FAMILY_APPEND) {
     if (reinterpret_cast<uintptr_t>(args->out) % 16)
       return fail(PA_ERR_INVALID_ARG, "out must be 16-byte aligned");

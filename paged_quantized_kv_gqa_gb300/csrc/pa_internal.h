@@ -16,6 +16,7 @@ namespace pa {
 
 constexpr int kItemWords = 8;        // b, kvh, token0, n_tok, causal_base, kv0, kv1, c|nch<<16
 constexpr int kDecodeRows = 64;      // packed (token, head) rows per decode tile
+constexpr int kWarpDecodeRows = 16;  // decode tiles up to this many rows run warp per item
 constexpr int kAppendRows = 256;     // packed rows per append item (two 128-row tiles)
 constexpr int kStatusBytes = 256;    // status block at the start of the workspace
 constexpr int64_t kDefaultWaitNs = 2000000000LL;
@@ -129,6 +130,9 @@ void set_error(const std::string& msg);
 // launchers (return a cudaError_t from the launch)
 cudaError_t launch_decode(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, cudaStream_t stream);
+// decode tiles of at most kWarpDecodeRows packed rows: warp-per-item kernel
+cudaError_t launch_decode_warp(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
+                               const CUtensorMap& tm_v, cudaStream_t stream);
 cudaError_t launch_append(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_k,
                           const CUtensorMap& tm_v, const CUtensorMap& tm_q, cudaStream_t stream);
 cudaError_t launch_mla(const Plan& plan, const AttnParams& p, const CUtensorMap& tm_c,

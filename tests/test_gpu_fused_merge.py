@@ -1,7 +1,11 @@
 """The decode kernel's opt-in in-kernel merge of split rows (the CTA that writes a row
 group's last chunk merges it): parity with the oracle, bit-identity with the
-separate merge kernel, counters that reset themselves between launches, and a
-bounded failure path."""
+separate merge kernel where both modes run the same attention kernel, counters
+that reset themselves between launches, and a bounded failure path.
+
+The in-kernel merge lives in the tensor-memory decode kernel; without it, tiles
+of at most 16 packed rows run the warp-per-item kernel instead, so for those
+cases the two modes agree with the oracle but not bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -39,8 +43,11 @@ def test_fused_merge_matches_oracle_and_separate_merge(kw):
     of, lf = _run(case, True)
     compare(case, of, lf, label=f"fused merge {kw}")
     os_, ls = _run(case, False)
-    assert np.array_equal(of.view(np.uint32), os_.view(np.uint32))
-    assert np.array_equal(lf.view(np.uint32), ls.view(np.uint32))
+    compare(case, os_, ls, label=f"separate merge {kw}")
+    rows = max(kw["seq_lens"]) * kw["q_heads"] // kw["kv_heads"]
+    if rows > 16:   # both modes run the tensor-memory kernel
+        assert np.array_equal(of.view(np.uint32), os_.view(np.uint32))
+        assert np.array_equal(lf.view(np.uint32), ls.view(np.uint32))
 
 
 def test_fused_merge_counters_reset_between_launches():
