@@ -2,19 +2,28 @@
 
 One step = the whole path over one batch: pa_run (attention over the paged
 int8 / FP8 cache, split-KV partials) + pa_merge (log-sum-exp merge), with the
-plan already uploaded and every input resident in HBM.  The default workload is
-decode-2 (bsz 64, q_len 1, 32 q heads / 8 kv heads, head dim 128, int8
-per-channel scales, prefix U[512, 4096], 4096-page shuffled pool, chunk 512);
-the metric is algorithmic KV-cache bytes (every visible (page, head) slab read
-once) per second.  --config 4 runs spec-verify-4 (same metric); --config 3 runs
-append-3 (chunked prefill, fp8 per-head, causal), whose metric is algorithmic
-FLOP/s (4 * D per visible (query head, position) pair) against the tensor peak.
+plan already uploaded and every input resident in HBM.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2|3|4|5] [--impl reference]
+By default every named workload runs, one after the other, and the single JSON
+line carries them all:
+  * the headline is decode-2 (bsz 64, q_len 1, 32 q heads / 8 kv heads, head
+    dim 128, int8 per-channel scales, prefix U[512, 4096], 4096-page shuffled
+    pool, chunk 512): its metric is algorithmic KV-cache bytes per second, the
+    bytes of every visible position's K and V rows read once (per token, not
+    rounded up to pages);
+  * config.per_workload holds one record per workload: decode-1 (latency in
+    microseconds: a two-sequence step is launch-bound), decode-2 and
+    spec-verify-4 (GB/s against the HBM copy peak), append-3 and mla-5
+    (algorithmic FLOP/s, 2 (Dqk + Dv) per visible (query head, position) pair,
+    against the tensor peak), each with its own roofline, end-to-end figure,
+    clock record and oracle CPU baseline.
+--config N runs one workload only (its record is then the headline).
 
-Prints one JSON line.  For N > 1 it runs under torch.distributed (one process
-per GPU); each rank runs an independent replica of the workload (the path has
-no cross-GPU exchange), time = max over ranks, value = all ranks' bytes / time.
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1..5] [--impl reference]
+
+For N > 1 it runs under torch.distributed (one process per GPU); each rank runs
+an independent replica of the workload (the path has no cross-GPU exchange),
+time = max over ranks, value = all ranks' work / time.
 """
 from __future__ import annotations
 
@@ -35,11 +44,14 @@ import numpy as np  # noqa: E402
 METRIC = "KV-cache HBM GB/s (decode) & TFLOP/s (append/MLA), % of GB300 roofline"
 L2_BYTES = 129 * 1000 * 1000          # GB300 L2 (129 MB)
 L2_FLUSH_BYTES = 512 << 20
+HEADLINE = 2
+ALL_WORKLOADS = (2, 1, 4, 3, 5)       # headline first
 
 
 def _peaks(bound: str):
     """(peak, source) for an HBM-bound (GB/s) or tensor-bound (TFLOP/s) kernel.
-    The fp16 kind::f16 tensor rate equals the bf16 one the peaks file measures."""
+    The fp16 kind::f16 tensor rate equals the bf16 one the peaks file measures;
+    a kernel timed alone takes the burst figure."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     key, fallback = ("hbm_gbs", 6800.0) if bound == "hbm" else ("bf16_tflops", 1900.0)
     if os.path.exists(p):
@@ -52,10 +64,9 @@ def _peaks(bound: str):
 
 # DRAM bytes (read + written) per launch of each attention kernel, from one
 # ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on the workload
-# (profiles/traffic_attention_kernels.md).  A figure is reported only while
-# the kernel's sources still hash to the version it was taken with.
+# (the kept ncu traffic summary under profiles/).  A figure is reported only
+# while the kernel's sources still hash to the version it was taken with.
 NCU_TRAFFIC = {
-    "decode-2": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "2dba40f4d753ecc7", 319.408384e6 + 4.340224e6),
     # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
     # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
     # states written both grow per sequence
@@ -83,8 +94,20 @@ def _traffic(workload: str):
     return int(ent[2])
 
 
-def _is_flops_workload(config: int) -> bool:
-    return config in (3, 5)
+def _kind(config: int) -> str:
+    """latency (decode-1), bytes (HBM-bound decode) or flops (tensor-bound)."""
+    return "latency" if config == 1 else "flops" if config in (3, 5) else "bytes"
+
+
+def algorithmic_bytes(case) -> int:
+    """KV bytes every visible position's K and V rows take, read once: per token
+    sum_b kvtot_b * Hkv * (Dqk + Dv) bytes (one byte per int8 / e4m3 element);
+    MLA reads each 576-byte latent row once (V is its prefix)."""
+    kvtot = case.kvtot.astype(np.int64)
+    kvtot = kvtot[np.asarray(case.seq_lens) > 0]
+    if case.layout == "mla":
+        return int(kvtot.sum()) * case.head_dim_qk
+    return int(kvtot.sum()) * case.kv_heads * (case.head_dim_qk + case.head_dim_v)
 
 
 def _dist():
@@ -92,14 +115,12 @@ def _dist():
     if ws <= 1:
         return 0, 1, 0
     import torch.distributed as dist
-    backend = "nccl"
-    dist.init_process_group(backend=backend)
+    dist.init_process_group(backend="nccl")
     return dist.get_rank(), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
 def _max_over_ranks(x: float, world: int, device: str = "cuda") -> float:
-    """Largest per-rank value (the step time the job is charged): NCCL on the
-    GPUs, gloo on the host."""
+    """Largest per-rank value (the step time the job is charged)."""
     if world <= 1:
         return x
     import torch
@@ -180,24 +201,106 @@ def _workload(config: int, bsz: int = 0):
     return synth.config(config, bsz)
 
 
-def run_cuda(args) -> dict:
+def synth_desc(n: int) -> str:
+    import synth
+    return synth.CONFIG_NAMES[n]
+
+
+# ---------------------------------------------------------------- CPU baseline
+# The fp64 oracle, as it stands, over (sequence, kv head) units on every host
+# core: a process pool forked before any CUDA call (the workers inherit the
+# host cases; a pool forked after CUDA initialisation would hang).
+_CASES = {}
+
+
+def _cpu_unit(key, b: int, h: int):
+    """One (sequence, kv head) unit of the oracle in a worker: its synthetic cache
+    pages are produced first (input generation, untimed), then the oracle runs
+    on them.  Returns (work in the metric's unit, seconds of the oracle)."""
+    from oracle import attention as oa
+    case = _CASES[key]
+    case._page_memo = {}
+    kvtot = int(case.seq_lens_kv[b]) + int(case.seq_lens[b])
+    for lb in range((kvtot + case.block_size - 1) // case.block_size):
+        pg = int(case.block_table[b, lb])
+        case.page_k(pg)
+        if case.layout != "mla":
+            case.page_v(pg)
+    t0 = time.perf_counter()
+    oa.unit_attention(case, b, h)
+    return _unit_work(case, b, _kind_of_case(case)), time.perf_counter() - t0
+
+
+def _kind_of_case(case) -> str:
+    return "flops" if case.name.startswith(("append", "mla")) else "bytes"
+
+
+def _unit_work(case, b: int, kind: str) -> float:
+    """Work of one (sequence, kv head) unit in the metric's unit (bytes or flops)."""
+    q, pre = float(case.seq_lens[b]), float(case.seq_lens_kv[b])
+    if q == 0:
+        return 0.0
+    if kind == "flops":   # visible (query head, position) pairs x 2 (Dqk + Dv)
+        G = case.q_heads // case.kv_heads
+        pairs = q * pre + q * (q + 1) / 2 if case.causal else q * (pre + q)
+        return pairs * G * 2 * (case.head_dim_qk + case.head_dim_v)
+    row = case.head_dim_qk if case.layout == "mla" else case.head_dim_qk + case.head_dim_v
+    return (pre + q) * row
+
+
+class CpuPool:
+    """Host cores running the oracle; created before the first GPU call."""
+
+    def __init__(self, cases: dict):
+        import multiprocessing as mp
+        _CASES.update(cases)
+        self.cores = os.cpu_count() or 1
+        self.pool = mp.get_context("fork").Pool(self.cores)
+
+    def close(self):
+        self.pool.terminate()
+        self.pool.join()
+
+    def baseline(self, key, seconds: float) -> dict:
+        """The oracle on a bounded sample: batches of one unit per core until
+        about `seconds` of oracle CPU time (summed over the cores) are spent;
+        the rate is the sample's work over the sum of the batches' wall times."""
+        case = _CASES[key]
+        kind = _kind_of_case(case)
+        units = [(b, h) for b in range(case.bsz) for h in range(case.kv_heads) if case.seq_lens[b] > 0]
+        np.random.default_rng(0).shuffle(units)
+        cpu_target = max(1.0, seconds)
+        done, n, i, wall, cpu = 0.0, 0, 0, 0.0, 0.0
+        while i < len(units) and cpu < cpu_target:
+            batch = units[i:i + self.cores]
+            i += len(batch)
+            got = self.pool.starmap(_cpu_unit, [(key, b, h) for b, h in batch])
+            done += sum(w for w, _ in got)
+            cpu += sum(t for _, t in got)
+            wall += max(t for _, t in got)     # the batch's units run side by side
+            n += len(batch)
+        dt = wall
+        scale, unit = (1e12, "TFLOP/s") if kind == "flops" else (1e9, "GB/s")
+        return {"value": round(done / dt / scale, 6), "unit": unit, "cores": self.cores,
+                "kind": "oracle",
+                "sample": f"{n} of {len(units)} (sequence, kv head) units of {case.name} in batches "
+                          f"of one unit per core: {cpu:.1f} s of oracle CPU time, {dt:.2f} s wall "
+                          f"(slowest unit of each batch) on {self.cores} processes, numpy fp64; the "
+                          f"synthetic cache pages are generated before each unit, untimed"}
+
+
+# ---------------------------------------------------------------- GPU workload
+def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dict:
+    """Times one workload; returns its record (the fields of the JSON line)."""
     import torch
     import paged_quantized_kv_gqa_gb300 as pa
     from synth.device import to_device
 
-    rank, world, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    case = _workload(args.config, args.bsz)
-    if args.tree_mask:
-        from synth.cases import tree_mask
-        case.attn_mask = tree_mask(case)
-        case.name += " tree-mask"
+    kind = _kind(cfg)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     d = to_device(case, dev)
     if args.fused_merge:
         pa.pa_set_fused_merge(True)
-        case.name += " fused-merge"
     plan = pa.pa_plan(pa.problem_of(case), case.seq_lens, case.seq_lens_kv, case.cu_seqlens_q, sms)
     pa.pa_set_fused_merge(False)
     desc = plan.describe()
@@ -210,19 +313,16 @@ def run_cuda(args) -> dict:
     stream = torch.cuda.current_stream(dev)
     pa.pa_plan_upload(plan, ws, stream)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    split = desc["max_chunks"] > 1
-
-    def step():
-        pa.pa_run(plan, cargs, ws, stream)
-        if split:
-            pa.pa_merge(plan, cargs, ws, stream)
+    split = desc["max_chunks"] > 1 and not desc["fused_merge"]
 
     for _ in range(args.warmup):
         flush.fill_(1)
-        step()
+        pa.pa_run(plan, cargs, ws, stream)
+        if split:
+            pa.pa_merge(plan, cargs, ws, stream)
     st, det = pa.pa_check(plan, ws, stream)
     if st != 0:
-        raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+        raise RuntimeError(f"{case.name}: device status {st} ({pa.pa_last_error()})")
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -245,18 +345,19 @@ def run_cuda(args) -> dict:
     run_ms = [a.elapsed_time(m) for a, m, _ in ev]
     ms = statistics.mean(step_ms)
     ms_max = _max_over_ranks(ms, world)
-    kv_bytes = desc["kv_bytes"]
-    flops_mode = _is_flops_workload(args.config)
-    # work per step in the metric's unit (GB or TFLOP)
-    work, unit, bound, runit = ((desc["flops"] / 1e12, "TFLOP/s", "tensor", "TFLOP/s")
-                                if flops_mode else (kv_bytes / 1e9, "GB/s", "hbm", "GB/s"))
-    value = _job_rate(work, world, ms_max)
     run_mean = statistics.mean(run_ms)
-    peak, peak_kind = _peaks(bound)
-    achieved = work / (run_mean * 1e-3)
     st, det = pa.pa_check(plan, ws, stream)
     if st != 0:
-        raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+        raise RuntimeError(f"{case.name}: device status {st} ({pa.pa_last_error()})")
+
+    kv_bytes = algorithmic_bytes(case)
+    if kind == "flops":
+        work, unit, bound = desc["flops"] / 1e12, "TFLOP/s", "tensor"
+    else:
+        work, unit, bound = kv_bytes / 1e9, "GB/s", "hbm"
+    peak, peak_kind = _peaks(bound)
+    achieved = work / (run_mean * 1e-3)
+    launches = K * (2 if split else 1)
 
     # end to end through the public API with host buffers, as a serving loop
     # runs it: every step uploads its inputs (q, block table, plan) from pinned
@@ -268,8 +369,8 @@ def run_cuda(args) -> dict:
     # memory.  L2 is not flushed in between; instead the steps rotate over enough
     # copies of the cache that more than twice the L2 size is read between two
     # uses of one copy (one copy when the cache alone is that large).
-    same_kv = d.get("cache_v") is None or d["cache_v"].data_ptr() == d["cache_k"].data_ptr()
-    n_rot = max(1, -(-2 * L2_BYTES // max(1, kv_bytes)))   # kv_bytes: cache bytes one step reads
+    same_kv = d["cache_v"].data_ptr() == d["cache_k"].data_ptr()
+    n_rot = max(1, -(-2 * L2_BYTES // max(1, kv_bytes)))
     caches = [(d["cache_k"], d["cache_v"])]
     for _ in range(n_rot - 1):
         ck = d["cache_k"].clone()
@@ -337,39 +438,98 @@ def run_cuda(args) -> dict:
     for sk in sets:                                 # every step's result is the path's result
         st, det = pa.pa_check(plan, sk["ws"], stream)
         if st != 0:
-            raise RuntimeError(f"device status {st} ({pa.pa_last_error()})")
+            raise RuntimeError(f"{case.name}: device status {st} ({pa.pa_last_error()})")
     if not torch.equal(sets[0]["out_h"].view(torch.int16), d["out"].cpu().view(torch.int16)):
-        raise RuntimeError("end-to-end output differs from the device-timed run")
-    e2e = _job_rate(work, world, _max_over_ranks(statistics.mean(e2e_ms), world))
+        raise RuntimeError(f"{case.name}: end-to-end output differs from the device-timed run")
+    e2e_step = _max_over_ranks(statistics.mean(e2e_ms), world)
 
-    res = {
-        "metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
-        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_max, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp16 (int8 / e4m3 KV dequantised exactly; fp32 accumulate)", "data": "synthetic",
-        "config": {"workload": case.name, "desc": synth_desc(args.config),
-                   "kv_bytes_per_step": kv_bytes, "flops_per_step": desc["flops"],
-                   "items": desc["num_items"],
-                   "ctas": desc["num_ctas"], "chunk": desc["chunk"],
-                   "l2": "flushed (512 MiB write) before every timed step",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": bound, "achieved": round(achieved, 1), "peak": peak,
-                     "unit": runit, "frac": round(achieved / peak, 4),
-                     "traffic": _traffic(case.name), "traffic_unit": "bytes per launch (ncu)",
-                     "peak_source": peak_kind, "kernel": "pa_run attention kernel",
-                     "run_ms": round(run_mean, 5)},
-        "e2e": {"value": round(e2e, 2), "unit": unit, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h),
-                "mode": "steps back to back: each step's upload and result read overlap the "
-                        "neighbouring steps' kernels (two buffer sets, copy streams)",
-                "l2": f"not flushed; steps rotate over {n_rot} cache cop{'y' if n_rot == 1 else 'ies'} "
-                      f"({kv_bytes / 1e6:.0f} MB read per step; > 2x L2 read between reuses)"},
-        "gpu_launches": K * (2 if split else 1),
-        "clocks": clk.summary(),
-    }
+    rec = {"workload": case.name, "desc": synth_desc(cfg), "steps": K, "warmup": args.warmup,
+           "ms_per_step": round(ms_max, 5), "kernel_ms": round(run_mean, 5),
+           "gpu_launches": launches, "clocks": clk.summary(),
+           "kv_bytes_per_step": kv_bytes, "flops_per_step": desc["flops"],
+           "items": desc["num_items"], "ctas": desc["num_ctas"], "chunk": desc["chunk"]}
+    roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
+            "traffic_unit": "bytes per launch (ncu)", "peak_source": peak_kind + " (of measured)"
+            if peak_kind.startswith("measured") else peak_kind,
+            "kernel": "pa_run attention kernel", "run_ms": round(run_mean, 5)}
+    if kind == "latency":
+        # two short sequences: the step is bound by launch latency, so it is
+        # reported as a latency; the byte rate is shown for reference only
+        rec.update(value=round(ms_max * 1e3, 2), unit="us", higher_is_better=False,
+                   e2e={"value": round(e2e_step * 1e3, 2), "unit": "us", "h2d_bytes_per_step": int(h2d),
+                        "d2h_bytes_per_step": int(d2h)})
+        roof["note"] = "launch-latency bound: the roofline fraction is not meaningful"
+    else:
+        rec.update(value=round(_job_rate(work, world, ms_max), 2), unit=unit, higher_is_better=True,
+                   e2e={"value": round(_job_rate(work, world, e2e_step), 2), "unit": unit,
+                        "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                        "mode": "steps back to back: each step's upload and result read overlap "
+                                "the neighbouring steps' kernels (two buffer sets, copy streams)",
+                        "l2": f"not flushed; steps rotate over {n_rot} cache "
+                              f"cop{'y' if n_rot == 1 else 'ies'} ({kv_bytes / 1e6:.0f} MB read per "
+                              f"step; > 2x L2 read between reuses)"})
+    rec["roofline"] = roof
+    if pool is not None:
+        rec["cpu_baseline"] = pool.baseline(case.name, args.cpu_seconds)
+    del sets, caches, d, ws, flush
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_cuda(args) -> dict:
+    import torch
+
+    rank, world, local = _dist()
+    configs = [args.config] if args.config else list(ALL_WORKLOADS)
+    cases = {}
+    for c in configs:
+        case = _workload(c, args.bsz)
+        if args.tree_mask:
+            from synth.cases import tree_mask
+            case.attn_mask = tree_mask(case)
+            case.name += " tree-mask"
+        cases[c] = case
+    pool = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(case, args.cpu_seconds, flops_mode)
+        pool = CpuPool({c.name: c for c in cases.values()})   # before the first CUDA call
+    try:
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+        records = {}
+        for c in configs:
+            records[c] = run_workload(c, cases[c], args, world, local, dev, pool)
+    finally:
+        if pool is not None:
+            pool.close()
+    head = records[configs[0]]
+    res = {
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": head["higher_is_better"], "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16 (int8 / e4m3 KV dequantised exactly; fp32 accumulate)", "data": "synthetic",
+        "config": config_of(configs[0], head, world,
+                            {records[c]["workload"]: records[c] for c in configs} if len(configs) > 1 else None),
+        "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+    }
+    if "cpu_baseline" in head:
+        res["cpu_baseline"] = head["cpu_baseline"]
     return res if rank == 0 else None
+
+
+def config_of(cfg: int, head: dict, world: int, per_workload=None) -> dict:
+    """The line's config: the same keys for the CUDA arm and the reference arm."""
+    c = {"workload": head["workload"] if head else synth_desc(cfg).split(":")[0],
+         "desc": synth_desc(cfg),
+         "l2": "flushed (512 MiB write) before every timed step",
+         "parallelism": f"replicas x{world}",
+         "algorithmic_unit": "KV bytes of every visible position read once (per token)"
+                             if _kind(cfg) != "flops" else
+                             "2 (Dqk + Dv) flop per visible (query head, position) pair"}
+    if per_workload is not None:
+        c["per_workload"] = per_workload
+    return c
 
 
 def run_cache_append(args) -> dict:
@@ -384,7 +544,7 @@ def run_cache_append(args) -> dict:
     rank, world, local = _dist()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    case = _workload(args.config)
+    case = _workload(args.config or 3)
     d = to_device(case, dev)
     k, v = new_kv(case)
     kd = torch.from_numpy(k.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -461,7 +621,6 @@ def run_cache_append(args) -> dict:
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         from oracle import cache_append as ca
         t0 = time.perf_counter()
-        n = 0
         sub = synth_subcase(case, max(1, case.bsz // 8))
         sk, sv = new_kv(sub)
         ca.cache_append(sub, sk, sv, sub.cache_k, sub.cache_v if sub.layout != "mla" else None)
@@ -483,63 +642,33 @@ def synth_subcase(case, nseq: int):
     return synth.make_case(**kw)
 
 
-def synth_desc(n: int) -> str:
-    import synth
-    return synth.CONFIG_NAMES[n]
-
-
-def cpu_baseline(case, seconds: float, flops_mode: bool = False) -> dict:
-    """The fp64 oracle as it stands, on a bounded sample of (sequence, kv head) units."""
-    from oracle import attention as oa
-    units = [(b, h) for b in range(case.bsz) for h in range(case.kv_heads)]
-    rng = np.random.default_rng(0)
-    rng.shuffle(units)
-    done_bytes = 0
-    G = case.q_heads // case.kv_heads
-
-    def per_unit(b):
-        q, pre = float(case.seq_lens[b]), float(case.seq_lens_kv[b])
-        if flops_mode:   # visible (query head, position) pairs x 2 (Dqk + Dv)
-            pairs = q * pre + q * (q + 1) / 2 if case.causal else q * (pre + q)
-            return pairs * G * 2 * (case.head_dim_qk + case.head_dim_v)
-        return int(np.ceil((pre + q) / case.block_size)) * case.block_size \
-            * (case.head_dim_qk + case.head_dim_v)
-    t0 = time.perf_counter()
-    n = 0
-    for b, h in units:
-        oa.unit_attention(case, b, h)
-        done_bytes += per_unit(b)
-        n += 1
-        if time.perf_counter() - t0 > seconds:
-            break
-    dt = time.perf_counter() - t0
-    per_s = done_bytes / dt / (1e12 if flops_mode else 1e9)
-    return {"value": round(per_s, 6), "unit": "TFLOP/s" if flops_mode else "GB/s",
-            "cores": 1, "kind": "oracle",
-            "sample": f"{n} of {len(units)} (sequence, kv head) units of {case.name}, "
-                      f"{dt:.1f} s, numpy fp64 (single-threaded gather/einsum)"}
-
-
 def run_reference(args) -> dict:
+    """The oracle, as it stands, on the host cores: the reference arm.  Every
+    step is a bounded sample of the same workload as the CUDA arm's line."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return None
-    case = _workload(args.config)
+    cfg = args.config or HEADLINE
+    case = _workload(cfg)
     K, W = args.steps, args.warmup
-    per = max(1.0, args.cpu_seconds / max(1, K + W))
-    flops_mode = _is_flops_workload(args.config)
-    vals = []
-    for i in range(W + K):
-        cb = cpu_baseline(case, per, flops_mode)
-        if i >= W:
-            vals.append(cb["value"])
+    pool = CpuPool({case.name: case})
+    try:
+        per = max(2.0, args.cpu_seconds)
+        vals = []
+        cb = None
+        for i in range(W + K):
+            cb = pool.baseline(case.name, per)
+            if i >= W:
+                vals.append(cb["value"])
+    finally:
+        pool.close()
     v = statistics.mean(vals)
     cb["value"] = round(v, 6)
     unit = cb["unit"]
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit,
             "n_gpus": 1, "steps": K, "warmup": W, "higher_is_better": True,
             "ms_per_step": None, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": case.name, "desc": synth_desc(args.config)},
+            "data": "synthetic", "config": config_of(cfg, {"workload": case.name}, 1),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -550,9 +679,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2, choices=[2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=0, choices=[0, 1, 2, 3, 4, 5],
+                    help="one workload only (0: all five, decode-2 as the headline)")
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=20.0,
+                    help="CPU work (summed over the host cores) of each oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tree-mask", action="store_true",
                     help="speculative verify with a seeded draft-tree mask (decode-family workloads)")
@@ -568,6 +699,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if (args.tree_mask or args.bsz or args.fused_merge) and not args.config:
+        ap.error("--tree-mask, --bsz and --fused-merge need --config")
     if args.op == "cache-append" and args.impl != "reference":
         res = run_cache_append(args)
     else:

@@ -1,9 +1,10 @@
 """Builds the CUDA library (libpa_gb300.so) in-tree with nvcc for sm_103a.
 
 Translation units compile in parallel, then link into one shared library next
-to this file.  The seeded input generator (synth/csrc) is built the same way
-into synth/libpa_synth.so.  Rebuilds only when a source is newer than the
-library.
+to this file.  The seeded input generators (synth/csrc) are built the same way:
+the device int8 generator into synth/libpa_synth.so (nvcc) and the threaded
+host normal generator into synth/libpa_synth_host.so (gcc).  Rebuilds only when
+a source is newer than the library.
 """
 from __future__ import annotations
 
@@ -19,6 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpa_gb300.so")
 SYNTH_SRC = os.path.join(ROOT, "synth", "csrc", "synth_gen.cu")
 SYNTH_LIB = os.path.join(ROOT, "synth", "libpa_synth.so")
+SYNTH_HOST_SRC = os.path.join(ROOT, "synth", "csrc", "synth_host.c")
+SYNTH_HOST_LIB = os.path.join(ROOT, "synth", "libpa_synth_host.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -76,6 +79,11 @@ def build(verbose: bool = False, force: bool = False) -> str:
         tmp = SYNTH_LIB + ".tmp"
         _run([nvcc, *ARCH, *FLAGS, "-shared", "-cudart", "shared", SYNTH_SRC, "-o", tmp])
         os.replace(tmp, SYNTH_LIB)
+    if force or _stale(SYNTH_HOST_LIB, [SYNTH_HOST_SRC]):
+        tmp = SYNTH_HOST_LIB + ".tmp"
+        _run([shutil.which("gcc") or "gcc", "-O2", "-fPIC", "-shared", "-pthread", SYNTH_HOST_SRC,
+              "-o", tmp, "-lm"])
+        os.replace(tmp, SYNTH_HOST_LIB)
     return LIB
 
 

@@ -130,10 +130,9 @@ class Case:
         held = self._cache_k if which == "k" else self._cache_v
         if held is not None:
             return held.reshape(-1)[start:start + count]
-        idx = np.arange(start, start + count, dtype=np.uint64)
         if self.kv_dtype == INT8:
             lo, hi = self.int8_range
-            return int8_to_bytes(rng.uniform_int(self.seed, stream, idx, lo, hi))
+            return rng.uniform_i8_bytes(self.seed, stream, start, count, lo, hi)
         full = self.cache_k if which == "k" else self.cache_v
         return full.reshape(-1)[start:start + count]
 

@@ -24,7 +24,12 @@ Derived draws:
                                   sqrt(-2 ln(1 - r0)) * cos(2 pi r1)
 
 The device generator in ``synth/csrc/synth_gen.cu`` implements the integer
-draw with the same formulas, so its bytes equal these bit for bit.
+draw with the same formulas, so its bytes equal these bit for bit.  Normal
+draws come from the threaded host library ``synth/csrc/synth_host.c`` (the same
+formulas in C, built next to this package) when it is present; its values and
+the numpy expression ``normal_np`` below agree to within two ulps (the two
+libraries' log1p / cos differ in the last bits), and every input of one run
+comes from the same one of the two.
 
 This module holds no attention arithmetic; it is shared by the oracle tests,
 the CUDA parity tests and the benchmark as the single source of inputs.
@@ -71,6 +76,21 @@ def uniform_int(seed: int, stream: int, idx, lo: int, hi: int) -> np.ndarray:
     return v.astype(np.int64) + lo
 
 
+def uniform_i8_bytes(seed: int, stream: int, start: int, count: int, lo: int, hi: int) -> np.ndarray:
+    """uniform_int draws for counters start .. start+count-1 as two's-complement
+    bytes (uint8); the threaded C generator when built (integer arithmetic:
+    the same bytes), else numpy."""
+    import os
+    lib = _host_lib()
+    if lib is not None and count > 0 and -128 <= lo <= hi <= 127:
+        out = np.empty(count, dtype=np.uint8)
+        lib.synth_uniform_i8(seed & 0xFFFFFFFFFFFFFFFF, stream, start, count, lo, hi, out.ctypes.data,
+                             min(32, os.cpu_count() or 1))
+        return out
+    v = uniform_int(seed, stream, np.arange(start, start + count, dtype=np.uint64), lo, hi)
+    return np.asarray(v, dtype=np.int64).astype(np.int8).view(np.uint8)
+
+
 def uniform01(seed: int, stream: int, idx) -> np.ndarray:
     """Reals uniform on [0, 1) with 53 random bits (float64)."""
     return (u64(seed, stream, idx) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
@@ -80,12 +100,52 @@ def uniform_real(seed: int, stream: int, idx, a: float, b: float) -> np.ndarray:
     return a + (b - a) * uniform01(seed, stream, idx)
 
 
-def normal(seed: int, stream: int, idx) -> np.ndarray:
+def normal_np(seed: int, stream: int, idx) -> np.ndarray:
     """Standard normal draws by Box-Muller on the counter pair (2i, 2i+1)."""
     i = np.asarray(idx, dtype=np.uint64)
     r0 = uniform01(seed, stream, i * np.uint64(2))
     r1 = uniform01(seed, stream, i * np.uint64(2) + np.uint64(1))
     return np.sqrt(-2.0 * np.log1p(-r0)) * np.cos(2.0 * np.pi * r1)
+
+
+_HOST = None
+
+
+def _host_lib():
+    """The threaded C generator, or None when it has not been built."""
+    global _HOST
+    if _HOST is None:
+        import ctypes
+        import os
+        path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa_synth_host.so")
+        if not os.path.exists(path):
+            return None
+        lib = ctypes.CDLL(path)
+        lib.synth_normal.argtypes = [ctypes.c_uint64] * 4 + [ctypes.c_void_p, ctypes.c_int]
+        lib.synth_normal.restype = ctypes.c_int
+        lib.synth_uniform_i8.argtypes = [ctypes.c_uint64] * 4 + [ctypes.c_int32, ctypes.c_int32,
+                                                                 ctypes.c_void_p, ctypes.c_int]
+        lib.synth_uniform_i8.restype = ctypes.c_int
+        _HOST = lib
+    return _HOST
+
+
+def normal(seed: int, stream: int, idx) -> np.ndarray:
+    """Standard normal draws by Box-Muller on the counter pair (2i, 2i+1).
+
+    Contiguous counter ranges go through the threaded C generator when it is
+    built; anything else (or no library) through ``normal_np``."""
+    import os
+    i = np.asarray(idx, dtype=np.uint64)
+    lib = _host_lib()
+    if lib is not None and i.ndim == 1 and i.size > 0:
+        start = int(i[0])
+        if int(i[-1]) - start == i.size - 1 and (i.size < 3 or np.all(np.diff(i) == 1)):
+            out = np.empty(i.size, dtype=np.float64)
+            lib.synth_normal(seed & 0xFFFFFFFFFFFFFFFF, stream, start, i.size, out.ctypes.data,
+                             min(32, os.cpu_count() or 1))
+            return out
+    return normal_np(seed, stream, i)
 
 
 def permutation(seed: int, stream: int, n: int) -> np.ndarray:
