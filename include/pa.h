@@ -271,7 +271,9 @@ pa_status pa_cache_append(const pa_plan_t* plan, const pa_args* args, const void
  *     before any GPU work.
  *   - No device memory is allocated or freed.  The first call on a device
  *     looks up the buffer's device address (cudaGetSymbolAddress with that
- *     device current); make that first call before any stream capture.
+ *     device current); make that first call before any stream capture.  The
+ *     address is kept per device and CUDA context: after a device reset (a new
+ *     primary context) the next call looks it up again.
  *   - All calls share the buffer, which keeps the last call's contents:
  *     calls that may overlap on the GPU (other streams, other host threads)
  *     race; serialise them.  The status word is cleared on every call.
@@ -293,9 +295,13 @@ pa_status pa_debug_gather(const pa_problem* problem, const pa_args* args, int32_
 
 /*
  * Test hook for failure detection.  wait_limit_ns bounds every mbarrier wait
- * inside the kernels (default 2e9 ns; 0 restores the default).  With
- * skip_first_load != 0 the next pa_run's loader skips its first page load so
- * the consumers' bounded wait runs out and the run records
+ * of one kernel role on another (default 2e9 ns; 0 restores the default;
+ * values below 1e6 ns are raised to 1e6 ns, since a working pipeline never
+ * waits a millisecond on one barrier).  The waits at a kernel's exit for
+ * copies and MMAs it has itself issued keep a fixed 2e9 ns bound, so no limit
+ * set here lets shared or tensor memory be released under work in flight.
+ * With skip_first_load != 0 the next pa_run's loader skips its first page
+ * load so the consumers' bounded wait runs out and the run records
  * PA_ERR_DEVICE_TIMEOUT (read it with pa_check).  Process-wide setting.
  */
 pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load);
@@ -305,10 +311,12 @@ pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load);
  * ctas * tiles_per_cta * 16 uint64 entries, later pa_run calls record
  * %globaltimer stamps (ns) of pipeline events: entry
  * [(cta * tiles_per_cta + tile) * 16 + event] for the first `ctas` CTAs and
- * their first `tiles_per_cta` KV tiles.  Events (decode kernel): 0 pages
- * issued, 1/2 K dequantisation start/end, 3 scores ready, 4 P ready,
- * 5/6 V dequantisation start/end, 7 V ready, 8 score MMA issued, 9 PV MMA
- * issued, 10 item epilogue done, 11 P buffer free.  NULL disables tracing.
+ * their first `tiles_per_cta` KV tiles.  Events (tensor-memory decode
+ * kernel): 0 pages issued, 1/2 K dequantisation start/end, 3 scores ready,
+ * 4 P ready, 5/6 V dequantisation start/end, 7 V ready, 8 score MMA issued,
+ * 9 PV MMA issued, 10 item epilogue done, 11 P buffer free.  Warp-per-item
+ * decode kernel (tile = the warp's n-th half page): event w = warp w finished
+ * it, 12 + w = it had landed (warps 0..3).  NULL disables tracing.
  * Process-wide setting.
  */
 pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta);

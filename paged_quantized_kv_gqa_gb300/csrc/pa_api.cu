@@ -620,7 +620,8 @@ pa_status pa_cache_append(const pa_plan_t* plan, const pa_args* args, const void
 pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load) {
   if (wait_limit_ns < 0) return fail(PA_ERR_INVALID_ARG, "negative wait limit");
   std::lock_guard<std::mutex> lk(g_fault_mu);
-  g_faults.wait_limit_ns = wait_limit_ns == 0 ? kDefaultWaitNs : wait_limit_ns;
+  // at least 1 ms: a healthy pipeline never waits that long on one barrier
+  g_faults.wait_limit_ns = wait_limit_ns == 0 ? kDefaultWaitNs : std::max<int64_t>(wait_limit_ns, kMinWaitNs);
   g_faults.skip_first_load = skip_first_load ? 1 : 0;
   return PA_OK;
 }

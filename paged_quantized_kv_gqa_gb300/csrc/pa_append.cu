@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every issued load lands before the CTA exits
       for (int s = 0; s < kStages; ++s)
-        if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, limit);
-      if (q_issued > 0) mbar_wait(qfull, (q_issued - 1) & 1, limit);
+        if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, kDrainNs);
+      if (q_issued > 0) mbar_wait(qfull, (q_issued - 1) & 1, kDrainNs);
     }
   } else if (warp == kWarpMmaS) {
     // ================================================================ S issue
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // drain: every MMA this warp issued completes before TMEM is released
       if (elect_one()) tc_commit(&drain[0]);
       __syncwarp();
-      mbar_wait(&drain[0], 0, limit);
+      mbar_wait(&drain[0], 0, kDrainNs);
     }
   } else if (warp == kWarpMmaPV) {
     // ================================================================ PV issue
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (elect_one()) tc_commit(&drain[1]);
       __syncwarp();
-      mbar_wait(&drain[1], 0, limit);
+      mbar_wait(&drain[1], 0, kDrainNs);
     }
   } else if (wg == 3) {
     // warp 15: no role (it completes the fourth warpgroup)

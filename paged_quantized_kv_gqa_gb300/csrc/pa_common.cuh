@@ -9,6 +9,11 @@
 
 namespace pa {
 
+// Bound on the exit drains: waits for copies and MMAs a CTA has already
+// issued, which complete on their own; fixed, so that no wait limit set for a
+// test can release shared or tensor memory under work still in flight.
+constexpr uint64_t kDrainNs = 2000000000ull;
+
 // First device error wins; the host reads it back through pa_check / pa_merge.
 __device__ __forceinline__ void record_status(int32_t* status, int code, int detail) {
   if (atomicCAS(status, 0, code) == 0) {

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       for (int s = 0; s < kStages; ++s)   // every issued load lands before exit
-        if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, limit);
+        if (issued_g[s] >= 0) mbar_wait(&full[s], ((uint32_t)issued_g[s] / kStages) & 1, kDrainNs);
     }
   } else if (warp == kWarpMma) {
     // ================================================================ MMA issue
@@ -317,9 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // drain: every issued MMA completes before TMEM is released
       for (int j = 0; j < 2; ++j)
-        if (s_commits[j]) mbar_wait(&sfull[j], (s_commits[j] - 1) & 1, limit);
+        if (s_commits[j]) mbar_wait(&sfull[j], (s_commits[j] - 1) & 1, kDrainNs);
       for (int j = 0; j < kPBufs; ++j)
-        if (pv_commits[j]) mbar_wait(&pvdone[j], (pv_commits[j] - 1) & 1, limit);
+        if (pv_commits[j]) mbar_wait(&pvdone[j], (pv_commits[j] - 1) & 1, kDrainNs);
     }
   } else if (wg == 3) {
     // ================================================================ fused merge

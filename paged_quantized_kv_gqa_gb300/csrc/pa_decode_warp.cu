@@ -53,7 +53,6 @@ constexpr int kWRing = 4;                  // item records between load and comp
 constexpr int kWMaxItems = 256;            // CTA item records kept in shared memory
 constexpr int kWScaleBytes = 4096;         // preloaded k / v scales (2 KB each)
 constexpr float kKOffset = 1152.0f;        // int8 K dequantised as 1152 + k
-constexpr uint64_t kDrainNs = 2000000000ull;   // bound on waits for this warp's own copies
 
 // Eight warps with three stages each: two half pages in flight per warp
 // cover the load latency, and eight warps split a CTA's items more evenly

@@ -20,6 +20,7 @@ constexpr int kWarpDecodeRows = 16;  // decode tiles up to this many rows run wa
 constexpr int kAppendRows = 256;     // packed rows per append item (two 128-row tiles)
 constexpr int kStatusBytes = 256;    // status block at the start of the workspace
 constexpr int64_t kDefaultWaitNs = 2000000000LL;
+constexpr int64_t kMinWaitNs = 1000000LL;      // floor of the test hook's wait limit
 
 // Status block layout (int32 words): [0] status code, [1] detail, [2] cta, [3] spare.
 

@@ -233,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       for (int s = 0; s < stages; ++s)
         if (issued_g[s] >= 0)
-          mbar_wait(&full[s], ((uint32_t)issued_g[s] / (uint32_t)stages) & 1, limit);
+          mbar_wait(&full[s], ((uint32_t)issued_g[s] / (uint32_t)stages) & 1, kDrainNs);
     }
   } else if (rank == 0 && warp == kWarpMma) {
     // ================================================================ S = Q' K^T (score CTA)
@@ -283,7 +283,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       (void)n_s;
       if (elect_one()) tc_commit(drain);   // every MMA issued completes before TMEM is released
       __syncwarp();
-      mbar_wait(drain, 0, limit);
+      mbar_wait(drain, 0, kDrainNs);
     }
   } else if (rank == 1 && warp == kWarpMma) {
     // ================================================================ O += P V (value CTA)
@@ -322,7 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok && lane == 0) raise_abort(PA_ERR_DEVICE_TIMEOUT, item_begin);
       if (elect_one()) tc_commit(drain);
       __syncwarp();
-      mbar_wait(drain, 0, limit);
+      mbar_wait(drain, 0, kDrainNs);
     }
   } else if (rank == 1 && warp == kWarpRelay) {
     // ================================================================ PV done -> score CTA

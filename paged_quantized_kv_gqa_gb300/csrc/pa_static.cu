@@ -15,7 +15,9 @@
 //   - the device address of the buffer is looked up once per device
 //     (cudaGetSymbolAddress, with that device current) by the first
 //     pa_run_static call on that device, so make that first call before any
-//     stream capture;
+//     stream capture; the address is kept together with the id of the CUDA
+//     context it belongs to, and looked up again when the current context is
+//     a different one (after cudaDeviceReset the module is loaded anew);
 //   - all calls share the one buffer and it keeps the last call's contents:
 //     calls whose work may overlap on the GPU (different streams, or several
 //     host threads) race with each other; serialise them;
@@ -35,9 +37,38 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_static_ws[kStaticWorkspaceBytes];
 
 std::mutex g_static_mu;
-void* g_static_ptr[kMaxDevices] = {};
+struct StaticSlot {
+  unsigned long long ctx_id;   // context the address belongs to (0: none yet)
+  void* ptr;
+};
+StaticSlot g_static[kMaxDevices] = {};
 
-// Device address of g_static_ws on the current device (looked up once).
+// Driver entry points for the current context's id (the runtime exposes none).
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of g_static_ws on the current device and context (looked up
+// once per device and context).
 pa_status static_workspace(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -49,17 +80,29 @@ pa_status static_workspace(void** out) {
     set_error("pa_run_static: device index out of range");
     return PA_ERR_UNSUPPORTED;
   }
+  // initialises the device's primary context if nothing is current yet
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) {
+    set_error(std::string("pa_run_static: context: ") + cudaGetErrorString(e));
+    return PA_ERR_CUDA;
+  }
+  unsigned long long ctx = 0;
+  if (!current_context_id(&ctx)) {
+    set_error("pa_run_static: cannot read the current CUDA context's id");
+    return PA_ERR_CUDA;
+  }
   std::lock_guard<std::mutex> lk(g_static_mu);
-  if (g_static_ptr[dev] == nullptr) {
+  if (g_static[dev].ptr == nullptr || g_static[dev].ctx_id != ctx) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_static_ws);
     if (e != cudaSuccess || ptr == nullptr) {
       set_error(std::string("pa_run_static: cudaGetSymbolAddress: ") + cudaGetErrorString(e));
       return PA_ERR_CUDA;
     }
-    g_static_ptr[dev] = ptr;
+    g_static[dev].ptr = ptr;
+    g_static[dev].ctx_id = ctx;
   }
-  *out = g_static_ptr[dev];
+  *out = g_static[dev].ptr;
   return PA_OK;
 }
 
