@@ -44,6 +44,43 @@ import numpy as np  # noqa: E402
 METRIC = "KV-cache HBM GB/s (decode) & TFLOP/s (append/MLA), % of GB300 roofline"
 L2_BYTES = 129 * 1000 * 1000          # GB300 L2 (129 MB)
 L2_FLUSH_BYTES = 512 << 20
+L2_DRAIN_BYTES = 256 << 20
+L2_NOTE = ("flushed before every timed step: 512 MiB written, then 256 MiB read so that the "
+           "flush's dirty lines are written back before the timed region, not during it")
+ROT_MAX = 8                           # most cache copies a step rotation may use
+
+
+def rotation(kv_bytes: int) -> int:
+    """Cache copies the timed steps rotate over: at least two (a step never
+    reads the copy the previous step read), and enough that more than twice
+    the L2 size is read between two uses of one copy; 0 when that would take
+    more than ROT_MAX copies (such a small workload is timed with a flush)."""
+    n = max(2, 1 + -(-2 * L2_BYTES // max(1, kv_bytes)))
+    return n if n <= ROT_MAX else 0
+
+
+def rotation_note(n_rot: int, kv_bytes: int) -> str:
+    if n_rot == 0:
+        return L2_NOTE
+    return (f"not flushed: inputs larger than L2; steps rotate over {n_rot} copies of the cache "
+            f"({kv_bytes / 1e6:.0f} MB read per step, so {(n_rot - 1) * kv_bytes / 1e6:.0f} MB "
+            f"> 2x L2 is read between two uses of one copy)")
+
+
+class L2Flush:
+    """Evicts the workload from L2 between timed steps: a write of a buffer four
+    times the L2 size, then a read of another twice its size, which pushes the
+    written (dirty) lines out to HBM before the next timed step starts."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(L2_DRAIN_BYTES // 8, dtype=torch.int64, device=dev)
+        self.sink = torch.empty(1, dtype=torch.int64, device=dev)
+
+    def __call__(self, i: int):
+        self.w.fill_(i & 0xFF)
+        self.sink.copy_(self.r.sum().view(1))
 HEADLINE = 2
 ALL_WORKLOADS = (2, 1, 4, 3, 5)       # headline first
 
@@ -312,33 +349,59 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
                          attn_mask=d.get("attn_mask"))
     stream = torch.cuda.current_stream(dev)
     pa.pa_plan_upload(plan, ws, stream)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     split = desc["max_chunks"] > 1 and not desc["fused_merge"]
+    kv_bytes = algorithmic_bytes(case)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        pa.pa_run(plan, cargs, ws, stream)
+    # the cache is not in L2 when a step starts: the steps rotate over copies
+    # of it (inputs larger than L2), or, for a workload too small for that,
+    # L2 is flushed before every step
+    n_rot = rotation(kv_bytes)
+    same_kv = d["cache_v"].data_ptr() == d["cache_k"].data_ptr()
+    caches = [(d["cache_k"], d["cache_v"])]
+    for _ in range(n_rot - 1):
+        ck = d["cache_k"].clone()
+        caches.append((ck, ck if same_kv else d["cache_v"].clone()))
+
+    def args_for(ck, cv, q, bt, out, lse):
+        return pa.make_args(q=q, cache_k=ck, cache_v=cv, k_scale=d["k_scale"],
+                            v_scale=d["v_scale"], block_table=bt, out=out, lse=lse,
+                            seq_lens=d["seq_lens"], seq_lens_kv=d["seq_lens_kv"],
+                            cu_seqlens_q=d["cu_seqlens_q"], attn_mask=d.get("attn_mask"))
+    rargs = [args_for(ck, cv, d["q"], d["block_table"], d["out"], d["lse"]) for ck, cv in caches]
+
+    def timed(K: int, flushed: bool):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+               torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            if flushed:
+                flush(i)                       # evict the cache from L2 between steps
+            a, m, b = ev[i]
+            ak = cargs if flushed else rargs[i % len(rargs)]
+            a.record(stream)
+            pa.pa_run(plan, ak, ws, stream)
+            m.record(stream)
+            if split:
+                pa.pa_merge(plan, ak, ws, stream)
+            b.record(stream)
+        return ev
+
+    for i in range(max(args.warmup, len(rargs))):
+        if n_rot == 0:
+            flush(1)
+        ak = rargs[i % len(rargs)]
+        pa.pa_run(plan, ak, ws, stream)
         if split:
-            pa.pa_merge(plan, cargs, ws, stream)
+            pa.pa_merge(plan, ak, ws, stream)
     st, det = pa.pa_check(plan, ws, stream)
     if st != 0:
         raise RuntimeError(f"{case.name}: device status {st} ({pa.pa_last_error()})")
 
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     _barrier(world)
     torch.cuda.synchronize(dev)
     with Clocks(local) as clk:
-        for i in range(K):
-            flush.fill_(i & 0xFF)              # evict the cache from L2 between steps
-            a, m, b = ev[i]
-            a.record(stream)
-            pa.pa_run(plan, cargs, ws, stream)
-            m.record(stream)
-            if split:
-                pa.pa_merge(plan, cargs, ws, stream)
-            b.record(stream)
+        ev = timed(K, n_rot == 0)
         torch.cuda.synchronize(dev)
     _barrier(world)
     step_ms = [a.elapsed_time(b) for a, _, b in ev]
@@ -349,8 +412,12 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
     st, det = pa.pa_check(plan, ws, stream)
     if st != 0:
         raise RuntimeError(f"{case.name}: device status {st} ({pa.pa_last_error()})")
-
-    kv_bytes = algorithmic_bytes(case)
+    # the same steps with L2 flushed before each (reported beside the number)
+    flushed_ms = None
+    if n_rot:
+        evf = timed(K, True)
+        torch.cuda.synchronize(dev)
+        flushed_ms = _max_over_ranks(statistics.mean(a.elapsed_time(b) for a, _, b in evf), world)
     if kind == "flops":
         work, unit, bound = desc["flops"] / 1e12, "TFLOP/s", "tensor"
     else:
@@ -366,20 +433,12 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
     # so step i+1's upload (copy stream) and step i-1's download (second copy
     # stream) overlap step i's kernels; events order each buffer's reuse.  The
     # timed region runs from the first upload to the last result in host
-    # memory.  L2 is not flushed in between; instead the steps rotate over enough
-    # copies of the cache that more than twice the L2 size is read between two
-    # uses of one copy (one copy when the cache alone is that large).
-    same_kv = d["cache_v"].data_ptr() == d["cache_k"].data_ptr()
-    n_rot = max(1, -(-2 * L2_BYTES // max(1, kv_bytes)))
-    caches = [(d["cache_k"], d["cache_v"])]
-    for _ in range(n_rot - 1):
-        ck = d["cache_k"].clone()
-        caches.append((ck, ck if same_kv else d["cache_v"].clone()))
+    # memory.  L2 is not flushed in between; the steps rotate over the same
+    # cache copies as the kernel-timed steps (a flush-timed workload, too small
+    # for a rotation, uses its one cache here).
     q_h = d["q"].cpu().pin_memory()
     bt_h = d["block_table"].cpu().pin_memory()
-    plan_words = (desc["num_ctas"] + 1) + desc["num_items"] * 8 + desc["total_q"] + \
-        len(desc["merge_tokens"])
-    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + plan_words * 4
+    h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + desc["plan_bytes"]
     d2h = d["out"].numel() * d["out"].element_size() + d["lse"].numel() * 4
     sets = []
     for k in range(2):
@@ -388,11 +447,7 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
         outk = torch.empty_like(d["out"])
         lsek = torch.empty_like(d["lse"])
         wsk = torch.zeros(plan.workspace_size, dtype=torch.uint8, device=dev)
-        ak = [pa.make_args(q=qk, cache_k=ck, cache_v=cv, k_scale=d["k_scale"],
-                           v_scale=d["v_scale"], block_table=btk, out=outk, lse=lsek,
-                           seq_lens=d["seq_lens"], seq_lens_kv=d["seq_lens_kv"],
-                           cu_seqlens_q=d["cu_seqlens_q"], attn_mask=d.get("attn_mask"))
-              for ck, cv in caches]
+        ak = [args_for(ck, cv, qk, btk, outk, lsek) for ck, cv in caches]
         sets.append(dict(q=qk, bt=btk, out=outk, lse=lsek, ws=wsk, args=ak,
                          out_h=torch.empty_like(d["out"], device="cpu").pin_memory(),
                          lse_h=torch.empty_like(d["lse"], device="cpu").pin_memory()))
@@ -418,7 +473,7 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
             stream.wait_event(ev_up[i])
             if i >= 2:
                 stream.wait_event(ev_down[i - 2])   # step i-2's result has left this set's out
-            ak = sk["args"][i % n_rot]
+            ak = sk["args"][i % len(caches)]
             pa.pa_run(plan, ak, sk["ws"], stream)
             if split:
                 pa.pa_merge(plan, ak, sk["ws"], stream)
@@ -447,7 +502,10 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
            "ms_per_step": round(ms_max, 5), "kernel_ms": round(run_mean, 5),
            "gpu_launches": launches, "clocks": clk.summary(),
            "kv_bytes_per_step": kv_bytes, "flops_per_step": desc["flops"],
-           "items": desc["num_items"], "ctas": desc["num_ctas"], "chunk": desc["chunk"]}
+           "items": desc["num_items"], "ctas": desc["num_ctas"], "chunk": desc["chunk"],
+           "l2": rotation_note(n_rot, kv_bytes)}
+    if flushed_ms is not None:
+        rec["flushed"] = {"ms_per_step": round(flushed_ms, 5), "l2": L2_NOTE}
     roof = {"bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
             "traffic_unit": "bytes per launch (ncu)", "peak_source": peak_kind + " (of measured)"
@@ -466,9 +524,8 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
                         "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                         "mode": "steps back to back: each step's upload and result read overlap "
                                 "the neighbouring steps' kernels (two buffer sets, copy streams)",
-                        "l2": f"not flushed; steps rotate over {n_rot} cache "
-                              f"cop{'y' if n_rot == 1 else 'ies'} ({kv_bytes / 1e6:.0f} MB read per "
-                              f"step; > 2x L2 read between reuses)"})
+                        "l2": f"not flushed; steps rotate over {len(caches)} cache "
+                              f"cop{'y' if len(caches) == 1 else 'ies'}"})
     rec["roofline"] = roof
     if pool is not None:
         rec["cpu_baseline"] = pool.baseline(case.name, args.cpu_seconds)
@@ -522,7 +579,7 @@ def config_of(cfg: int, head: dict, world: int, per_workload=None) -> dict:
     """The line's config: the same keys for the CUDA arm and the reference arm."""
     c = {"workload": head["workload"] if head else synth_desc(cfg).split(":")[0],
          "desc": synth_desc(cfg),
-         "l2": "flushed (512 MiB write) before every timed step",
+         "l2": (head or {}).get("l2", L2_NOTE),
          "parallelism": f"replicas x{world}",
          "algorithmic_unit": "KV bytes of every visible position read once (per token)"
                              if _kind(cfg) != "flops" else
@@ -559,11 +616,11 @@ def run_cache_append(args) -> dict:
                          seq_lens_kv=d["seq_lens_kv"], cu_seqlens_q=d["cu_seqlens_q"])
     stream = torch.cuda.current_stream(dev)
     pa.pa_plan_upload(plan, ws, stream)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     vals = kd.numel() + (0 if vd is None else vd.numel())
     nbytes = vals * 3                      # bf16 read + one stored byte each
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush(1)
         pa.pa_cache_append(plan, cargs, kd, vd, stride, ws, stream)
     st, _ = pa.pa_check(plan, ws, stream)
     if st != 0:
@@ -575,7 +632,7 @@ def run_cache_append(args) -> dict:
     torch.cuda.synchronize(dev)
     with Clocks(local) as clk:
         for i in range(K):
-            flush.fill_(i & 0xFF)
+            flush(i)
             ev[i][0].record(stream)
             pa.pa_cache_append(plan, cargs, kd, vd, stride, ws, stream)
             ev[i][1].record(stream)
@@ -590,7 +647,7 @@ def run_cache_append(args) -> dict:
     sth = torch.empty(4, dtype=torch.int32).pin_memory()
     e2e_ms = []
     for i in range(max(3, K)):
-        flush.fill_(i & 0xFF)
+        flush(i)
         a, b = ev[i % K]
         a.record(stream)
         kd.copy_(kh, non_blocking=True)
@@ -608,7 +665,7 @@ def run_cache_append(args) -> dict:
         "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 quotient -> int8 / e4m3 bytes", "data": "synthetic",
         "config": {"workload": case.name + " appended tokens", "tokens": case.total_q,
-                   "bytes_per_step": nbytes, "l2": "flushed (512 MiB write) before every timed step",
+                   "bytes_per_step": nbytes, "l2": L2_NOTE,
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": round(work / (ms * 1e-3), 1), "peak": peak,
                      "unit": "GB/s", "frac": round(work / (ms * 1e-3) / peak, 4), "traffic": None,
@@ -668,7 +725,8 @@ def run_reference(args) -> dict:
     return {"impl": "reference", "metric": METRIC, "value": round(v, 6), "unit": unit,
             "n_gpus": 1, "steps": K, "warmup": W, "higher_is_better": True,
             "ms_per_step": None, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(cfg, {"workload": case.name}, 1),
+            "data": "synthetic", "config": config_of(cfg, {"workload": case.name,
+                                                                 "l2": "host CPU run (no GPU L2)"}, 1),
             "cpu_baseline": cb,
             "e2e": {"value": round(v, 6), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

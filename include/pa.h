@@ -170,6 +170,8 @@ typedef struct pa_plan_desc {
   double flops;             /* 2*(Dqk+Dv) per visible (position, query head)  */
   int32_t fused_merge;      /* 1: pa_run merges the split rows itself (decode
                                family), pa_merge does nothing               */
+  size_t plan_bytes;        /* bytes pa_plan_upload copies to the device
+                               (after the 256-byte status block)             */
 } pa_plan_desc;
 
 /*

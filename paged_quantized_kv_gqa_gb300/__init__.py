@@ -57,7 +57,8 @@ class PaPlanDesc(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("kv_bytes", ctypes.c_int64),
         ("flops", ctypes.c_double),
-        ("fused_merge", ctypes.c_int32)]
+        ("fused_merge", ctypes.c_int32),
+        ("plan_bytes", ctypes.c_size_t)]
 
 
 def _load():
@@ -181,7 +182,8 @@ class Plan:
                     nch_token=arr(d.nch_token, d.total_q),
                     merge_tokens=arr(d.merge_tokens, d.n_merge),
                     workspace_bytes=int(d.workspace_bytes), kv_bytes=int(d.kv_bytes),
-                    flops=float(d.flops), fused_merge=bool(d.fused_merge))
+                    flops=float(d.flops), fused_merge=bool(d.fused_merge),
+                    plan_bytes=int(d.plan_bytes))
 
     @property
     def workspace_size(self) -> int:

@@ -416,6 +416,7 @@ pa_status pa_plan_describe(const pa_plan_t* plan, pa_plan_desc* d) {
   d->kv_bytes = plan->kv_bytes;
   d->flops = plan->flops;
   d->fused_merge = plan->fused_merge ? 1 : 0;
+  d->plan_bytes = plan->plan_bytes;
   return PA_OK;
 }
 

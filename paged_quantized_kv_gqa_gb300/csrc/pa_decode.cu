@@ -65,6 +65,9 @@ constexpr int kWarpTma = 12;
 constexpr int kWarpMma = 13;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kPBufs = 4;                        // P^T ring depth
+// P^T buffer: [128 positions][64 rows] fp16, MN-major (rows contiguous),
+// 128-byte swizzle; a thread (= position) writes its rows with 16-byte stores
+constexpr int kPBufBytes = kTileTok * 128;
 constexpr int kMergeRows = 2;                    // rows a merge warp combines at once
 
 // The decode pipeline is latency-bound: its waits re-probe every 32 ns.
@@ -87,7 +90,7 @@ struct Smem {
   static constexpr int kStages = stages_for(NR);
   static constexpr int kQ = kStages * kStageBytes;         // Q'[2]
   static constexpr int kP = kQ + 2 * NR * 256;             // P^T ring
-  static constexpr int kRed = kP + kPBufs * NR * 256;      // [4][NR] warp maxima
+  static constexpr int kRed = kP + kPBufs * kPBufBytes;    // [4][NR] warp maxima
   static constexpr int kRedL = kRed + 4 * NR * 4;          // [4][NR] warp row sums
   static constexpr int kLsum = kRedL + 4 * NR * 4;         // [2][NR] 1/l per item (by parity)
   static constexpr int kM = kLsum + 2 * NR * 4;            // [NR] running max
@@ -252,6 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // elected lane issues the MMAs and commits
     {
       const uint32_t idesc = idesc_f16_f32(128, NR);
+      const uint32_t idesc_pv = idesc_f16_f32_bmn(128, NR);   // B = P^T, MN-major
       TileCursor cs, cp;       // next S to issue, next PV to issue
       cs.init(p.items, item_begin, item_end);
       cp.init(p.items, item_begin, item_end);
@@ -285,13 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_test_wait(&vready[gp & 1], (gp >> 1) & 1)) {
           tc_fence_after();
           const uint32_t vb = TM::V0 + (gp & 1) * 64;
-          const uint32_t pb = p_s + (gp & 3) * NR * 256;
+          const uint32_t pb = p_s + (gp & 3) * kPBufBytes;
           const uint32_t od = TM::O0 + ((cp.it - item_begin) & 1) * NR;
           if (elect_one()) {
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t bd = sdesc_k128(pb + (kk >> 2) * NR * 128 + (kk & 3) * 32);
-              mma_ts(tmem + od, tmem + vb + 8 * kk, bd, idesc, (cp.i > 0 || kk > 0) ? 1u : 0u);
+              // positions 16kk .. 16kk+15: two 8-position swizzle atoms of 1 KB
+              const uint64_t bd = sdesc_mn128(pb + kk * 2048, kPBufBytes, 1024);
+              mma_ts(tmem + od, tmem + vb + 8 * kk, bd, idesc_pv, (cp.i > 0 || kk > 0) ? 1u : 0u);
             }
             tc_commit(&pvdone[gp & 3]);
           }
@@ -474,6 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int j = 0; j < NH; ++j) l[j] = 0.0f;
+      bool m_ninf = false;   // some row of this half has m = -inf (warpgroup-uniform)
       for (int i = 0; i < cur.ntiles; ++i, ++g) {
         // ---- S_g columns of this half -> registers, then release the S buffer
         float s[NH];
@@ -496,11 +502,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         warp_arrive(&sfree[g & 1], lane);
 
-        // ---- x = s * c (log2 units), -inf where masked
+        // ---- x = s * c - m: log2 units, relative to the row's running max m,
+        // -inf where masked.  The first tile of an item, and every tile while
+        // some row of this half has seen no visible position yet (m = -inf),
+        // take the general path, which forms x once the new maximum is known.
         const int tpos0 = cur.kv0 + i * kTileTok;
         const int jpos = tpos0 + pos_in_tile;
         const bool need_mask = (tpos0 + kTileTok > cur.kv1) || (tpos0 + kTileTok - 1 > cur.cbase) ||
                                (TREE && tpos0 + kTileTok > pre_len);
+        const bool general = (i == 0) || m_ninf;
+        const float4* m4s = reinterpret_cast<const float4*>(m_s + r_lo);
+        bool exceed = general;
         if (need_mask) {
           const int lim_tok = jpos - cur.cbase;   // visible for rows of token >= lim_tok
           const bool tree = TREE && jpos >= pre_len && jpos < cur.kv1;
@@ -514,20 +526,48 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             s[j] = vis ? s[j] * c_log2 : -INFINITY;
           }
+          if (!general) {
+#pragma unroll
+            for (int j4 = 0; j4 < NH / 4; ++j4) {
+              const float4 m4 = m4s[j4];
+              const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                s[4 * j4 + e] -= mv[e];
+                exceed |= s[4 * j4 + e] > kTau;
+              }
+            }
+          }
+        } else if (!general) {
+#pragma unroll
+          for (int j4 = 0; j4 < NH / 4; ++j4) {
+            const float4 m4 = m4s[j4];
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              s[4 * j4 + e] = fmaf(s[4 * j4 + e], c_log2, -mv[e]);
+              exceed |= s[4 * j4 + e] > kTau;
+            }
+          }
         } else {
 #pragma unroll
           for (int j = 0; j < NH; ++j) s[j] *= c_log2;
         }
-        // the first tile of an item always sets the running max
-        bool exceed = (i == 0);
-        if (i > 0) {
-#pragma unroll
-          for (int j = 0; j < NH; ++j)
-            if (r_lo + j < n_rows) exceed |= (s[j] - m_s[r_lo + j] > kTau);
-        }
+        // padded rows have Q' = 0, so x = 0 - 0 there and they never exceed
         const bool resc = bar_or(bar_id, 128, exceed);
         if (*my_abort) { fail = true; stop = true; break; }
         if (resc) {
+          if (!general) {
+            // back to s * c (-inf stays -inf)
+#pragma unroll
+            for (int j4 = 0; j4 < NH / 4; ++j4) {
+              const float4 m4 = m4s[j4];
+              s[4 * j4 + 0] += m4.x;
+              s[4 * j4 + 1] += m4.y;
+              s[4 * j4 + 2] += m4.z;
+              s[4 * j4 + 3] += m4.w;
+            }
+          }
           // exact tile maximum per row, new running max; rescale l (registers)
           // and this half's columns of O (TMEM) by 2^(m_old - m_new)
 #pragma unroll
@@ -570,7 +610,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_wait_st();
             }
           }
-          bar_sync(bar_id, 128);  // red / alpha_s are reused by the next rescale
+          // x against the new maximum; a row with no visible position so far
+          // (m = -inf) has only x = -inf
+          m_ninf = false;
+#pragma unroll
+          for (int j4 = 0; j4 < NH / 4; ++j4) {
+            const float4 m4 = m4s[j4];
+            const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              m_ninf |= mv[e] == -INFINITY;
+              s[4 * j4 + e] -= mv[e] == -INFINITY ? 0.0f : mv[e];
+            }
+          }
+          bar_sync(bar_id, 128);  // red / alpha_s / m_s are reused by the next rescale
         }
         // P^T slot g&3 was last read by PV_{g-4}
         if (g >= kPBufs && !fail &&
@@ -578,29 +631,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           note_fail(it);
         if (tid == 0) trace_ev(p, g, 11);
         {
-          // even lanes store row r, odd lanes row r + 4 (disjoint bank groups)
-          uint32_t* pw = reinterpret_cast<uint32_t*>(smem + SM::kP + (g & 3) * NR * 256);
-          const bool odd = lane & 1;
-          const int tt = pos_in_tile & ~1;
-          const int base = (tt >> 6) * NR * 128 + ((tt & 7) * 2);
-          const int chunk16 = (tt & 63) >> 3;
+          // p = 2^x (0 where masked); this position's row of P^T: 16-byte
+          // chunk c (rows 8c .. 8c+7) at chunk c ^ (position & 7)
+          const uint32_t prow = p_s + (g & 3) * kPBufBytes + (pos_in_tile >> 3) * 1024 +
+                                (pos_in_tile & 7) * 128;
 #pragma unroll
-          for (int j0 = 0; j0 < NH; j0 += 8) {
-            float mr[8];
+          for (int cc = 0; cc < NH / 8; ++cc) {
+            float pv[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) mr[k] = m_s[r_lo + j0 + k];
-#pragma unroll
-            for (int j1 = 0; j1 < 4; ++j1) {
-              const int j = j0 + j1;
-              const float p0 = s[j] == -INFINITY ? 0.f : fast_exp2(s[j] - mr[j1]);
-              const float p1 = s[j + 4] == -INFINITY ? 0.f : fast_exp2(s[j + 4] - mr[j1 + 4]);
-              l[j] += p0;
-              l[j + 4] += p1;
-              const float recv = __shfl_xor_sync(0xffffffffu, odd ? p0 : p1, 1);
-              const int rr = r_lo + (odd ? j + 4 : j);
-              const uint32_t word = odd ? pack_half2(recv, p1) : pack_half2(p0, recv);
-              pw[(base + rr * 128 + ((chunk16 ^ (rr & 7)) << 4)) >> 2] = word;
+            for (int e = 0; e < 8; ++e) {
+              pv[e] = fast_exp2(s[8 * cc + e]);
+              l[8 * cc + e] += pv[e];
             }
+            const int chunk = wg * (NH / 8) + cc;
+            st_shared_v4(prow + ((chunk ^ (pos_in_tile & 7)) << 4),
+                         make_uint4(pack_half2(pv[0], pv[1]), pack_half2(pv[2], pv[3]),
+                                    pack_half2(pv[4], pv[5]), pack_half2(pv[6], pv[7])));
           }
           fence_proxy_async_smem();
         }
