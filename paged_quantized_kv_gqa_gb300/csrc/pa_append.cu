@@ -531,15 +531,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t st = s_base + SM::kRaw + stage * kStageBytes;
         if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
         const int nvalid = min(kTile, m.kv1 - (m.kv0 + i * kTile));
-        // ---- K: thread t converts position t >> 1, dims 64 (t & 1) .. +63,
-        // into K16 buffer g&1 (free once both chains' S of page g-2 completed)
+        // ---- K: thread t converts position t & 63, dims 64 (t >> 6) .. +63,
+        // into K16 buffer g&1 (free once both chains' S of page g-2 completed);
+        // eight neighbouring threads take eight rows, so each 16-byte store
+        // phase covers all 32 banks
         if (g >= 2 && !wait_or_abort(&kfree[g & 1], ((g - 2) >> 1) & 1, limit, abort_any)) {
           note_fail(it);
           break;
         }
         if (t == 0) trace_ev(p, g, 1);
         {
-          const int row = t >> 1, half = t & 1;
+          const int row = t & 63, half = t >> 6;
           const uint32_t src = st + row * 128;
           const uint32_t dst = k16 + (g & 1) * kK16Bytes + half * kTile * 128 + row * 128;
 #pragma unroll
