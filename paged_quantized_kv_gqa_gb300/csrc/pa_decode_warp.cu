@@ -51,6 +51,7 @@ constexpr int kWKBytes = kWHalf * kWDim;   // K bytes of a stage
 constexpr int kWStage = 2 * kWKBytes;      // K + V^T of a half page
 constexpr int kWRing = 4;                  // item records between load and compute cursors
 constexpr int kWMaxItems = 256;            // CTA item records kept in shared memory
+constexpr int kWBtStride = 8;              // block-table entries kept per item (512 positions)
 constexpr int kWScaleBytes = 4096;         // preloaded k / v scales (2 KB each)
 constexpr float kKOffset = 1152.0f;        // int8 K dequantised as 1152 + k
 
@@ -67,7 +68,8 @@ struct WCfg {
   static constexpr int kBarOff = kItemOff + kWMaxItems * kItemWords * 4;   // [warps][stages]
   static constexpr int kRecOff = kBarOff + kWarps * kStages * 8;    // [warps][ring][12] int32
   static constexpr int kMiscOff = kRecOff + kWarps * kWRing * 48;   // next item, abort
-  static constexpr int kTotal = kMiscOff + 16 + 1024;               // + alignment slack
+  static constexpr int kBtOff = kMiscOff + 16;                      // [kWMaxItems][kWBtStride] int32
+  static constexpr int kTotal = kBtOff + kWMaxItems * kWBtStride * 4 + 1024;   // + alignment slack
   static_assert(kTotal <= 232448, "shared memory overflow");
 };
 
@@ -91,6 +93,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
+}
+
+__device__ __forceinline__ uint32_t pack_bf162(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
@@ -144,6 +151,7 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOff) + warp * C::kStages;
   int32_t* items_s = reinterpret_cast<int32_t*>(smem + C::kItemOff);
+  int32_t* bt_s = reinterpret_cast<int32_t*>(smem + C::kBtOff);
   int32_t* rec_ring = reinterpret_cast<int32_t*>(smem + C::kRecOff) + warp * kWRing * 12;
   int* next_item = reinterpret_cast<int*>(smem + C::kMiscOff);
   volatile int* abort_any = reinterpret_cast<volatile int*>(smem + C::kMiscOff + 4);
@@ -167,6 +175,7 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
     const int n_it = min(item_end - item_begin, kWMaxItems) * kItemWords;
     for (int i = threadIdx.x; i < n_it; i += blockDim.x) items_s[i] = p.items[(int64_t)item_begin * kItemWords + i];
   }
+  const int n_staged = min(item_end - item_begin, kWMaxItems);
   if (sc_smem) {
     __nv_bfloat16* kd = reinterpret_cast<__nv_bfloat16*>(smem + C::kScaleOff);
     __nv_bfloat16* vd = kd + kWScaleBytes / 4;
@@ -176,6 +185,19 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
       kd[i] = kg[i];
       vd[i] = vg[i];
     }
+  }
+  __syncthreads();
+  // The page ids of every staged item of at most kWBtStride pages, so that a
+  // warp moving to its next item issues that item's first copies at once
+  // instead of first waiting for a block-table read from memory (all warps
+  // move at about the same time, and such a wait drains every warp's ring).
+  for (int idx = threadIdx.x; idx < n_staged * kWBtStride; idx += blockDim.x) {
+    const int32_t* rec = items_s + (idx / kWBtStride) * kItemWords;
+    const int k = idx % kWBtStride;
+    const int kv0 = rec[5];
+    const int np = (rec[6] - kv0 + kWPage - 1) / kWPage;
+    const int nb = p.max_blocks - kv0 / kWPage;   // entries left in the sequence's row
+    bt_s[idx] = k < np && k < nb ? p.block_table[(int64_t)rec[0] * p.max_blocks + kv0 / kWPage + k] : -1;
   }
   __syncthreads();
 
@@ -188,6 +210,30 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
   int cur_it = -1, cur_b = 0, cur_kvh = 0, cur_kv0 = 0, cur_nh = 0, cur_h = 0;
   int cur_bt = -1, nxt_bt = -1;       // lane k: page id of page 32 * batch + k of the item
   int pend_it = -1, pend_rec = 0, pend_bt = -1;
+  // Q rows of a taken item, read when the item is taken (several stages
+  // before its compute starts) so that their latency is off the critical
+  // path; lane (g, t) holds dims 64 h + 16 t .. +15 of row 8 j + g
+  uint4 qpre[NB][2][2];
+  int qpre_it = -1;
+  auto load_q_rows = [&](uint4 (&qr)[NB][2][2], int tok0, int ntok, int kvh) {
+    const int n_rows = ntok * G;
+#pragma unroll
+    for (int j = 0; j < NB; ++j) {
+      const int row = 8 * j + g;
+      const bool valid = row < n_rows;
+      const __nv_bfloat16* qrow = p.q + (int64_t)(tok0 + (valid ? row / G : 0)) * p.q_stride +
+                                  (int64_t)(kvh * G + (valid ? row % G : 0)) * kWDim;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int d0 = 64 * h + 16 * t;
+        qr[j][h][0] = qr[j][h][1] = make_uint4(0, 0, 0, 0);
+        if (valid) {
+          qr[j][h][0] = __ldg(reinterpret_cast<const uint4*>(qrow + d0));
+          qr[j][h][1] = __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8));
+        }
+      }
+    }
+  };
   uint32_t n_load = 0;                // half pages issued by this warp
   uint32_t k_load = 0;                // items started on the load side
   // failure-detection test hook: the first half page of the CTA's first item
@@ -214,7 +260,15 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
       const int kv0 = __shfl_sync(0xffffffffu, pend_rec, 5);
       const int kv1 = __shfl_sync(0xffffffffu, pend_rec, 6);
       const int np = (kv1 - kv0 + kWPage - 1) / kWPage;
-      pend_bt = lane < np ? bt_at(b, kv0, lane) : -1;
+      if (pend_it - item_begin < n_staged && np <= kWBtStride)
+        pend_bt = lane < np ? bt_s[(pend_it - item_begin) * kWBtStride + lane] : -1;
+      else
+        pend_bt = lane < np ? bt_at(b, kv0, lane) : -1;
+      if (qpre_it < 0) {   // the previous prefetch has been used
+        load_q_rows(qpre, __shfl_sync(0xffffffffu, pend_rec, 2), __shfl_sync(0xffffffffu, pend_rec, 3),
+                    __shfl_sync(0xffffffffu, pend_rec, 1));
+        qpre_it = pend_it;
+      }
     }
   };
   // issues the next half page of this warp's sequence; false when none is left
@@ -309,22 +363,26 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
     // D = 16 (t + 4 (ks >> 2)) + 4 (ks & 3); cs = the row's int8-K offset term
     uint32_t qf[NB][8][2];
     float cs[NB][2];
+    uint4 qr[NB][2][2];
+    if (it == qpre_it) {
+#pragma unroll
+      for (int j = 0; j < NB; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          qr[j][h][0] = qpre[j][h][0];
+          qr[j][h][1] = qpre[j][h][1];
+        }
+      qpre_it = -1;
+    } else {
+      load_q_rows(qr, m.tok0, m.ntok, m.kvh);
+    }
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
-      const int row = 8 * j + g;
-      const bool valid = row < n_rows;
-      const int token = m.tok0 + (valid ? row / G : 0);
-      const int head = m.kvh * G + (valid ? row % G : 0);
-      const __nv_bfloat16* qrow = p.q + (int64_t)token * p.q_stride + (int64_t)head * kWDim;
       float qsum = 0.f;
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         const int d0 = 64 * half + 16 * t;
-        uint4 r0 = make_uint4(0, 0, 0, 0), r1 = r0;
-        if (valid) {
-          r0 = __ldg(reinterpret_cast<const uint4*>(qrow + d0));
-          r1 = __ldg(reinterpret_cast<const uint4*>(qrow + d0 + 8));
-        }
+        const uint4 r0 = qr[j][half][0], r1 = qr[j][half][1];
         const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
         float f[16];
 #pragma unroll
@@ -518,20 +576,23 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
         }
       }
 
-      // the stage is free: load this warp's next half page into it
+      // the stage is free: load this warp's next half page into it (after
+      // the epilogue for the item's last half page: the epilogue stages the
+      // output rows there)
       __syncwarp();
       if (lane == 0) trace_ev(p, n_comp, warp);
       ++n_comp;
-      issue_next();
+      if (hp + 1 < nh) issue_next();
     }
     if (fail) break;
 
-    // ---- epilogue: row sums over the warp, then out + lse or the partial state
-    const float vs_head = p.scale_kind == PA_SCALE_GLOBAL ? reinterpret_cast<const float*>(p.v_scale)[0]
-                          : p.scale_kind == PA_SCALE_PER_KV_HEAD
-                              ? __bfloat162float(sc_smem ? vs_s[m.kvh]
-                                                         : reinterpret_cast<const __nv_bfloat16*>(p.v_scale)[m.kvh])
-                              : 1.f;
+    // ---- epilogue.  Row sums over the warp; O / l goes through the stage of
+    // the item's last half page (fp32 [8 NB rows][128 dims], the dims of row
+    // r XOR-swizzled by 8 ((r >> 1) & 3) so that both passes are free of bank
+    // conflicts) and leaves as 16-byte row pieces.  A compact loop keeps the
+    // code that every warp runs at about the same moment small.
+    float* stg = reinterpret_cast<float*>(smem + C::kStageOff +
+                                          (warp * C::kStages + (n_comp - 1) % C::kStages) * kWStage);
 #pragma unroll
     for (int j = 0; j < NB; ++j) {
 #pragma unroll
@@ -541,35 +602,17 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
         l += __shfl_xor_sync(0xffffffffu, l, 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         const int r = 8 * j + 2 * t + e;
-        if (r >= n_rows) continue;
-        const int token = m.tok0 + r / G;
-        const int head = m.kvh * G + r % G;
         const float inv = l > 0.f ? __frcp_rn(l) : 0.f;
-        const float ln2 = 0.69314718055994530942f;
-        const float mr = mrow[j][e];   // true running max (log2 units, offset term removed)
 #pragma unroll
         for (int d = 0; d < 8; ++d)
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int dim = 16 * d + g + 8 * h;
-            float vs = vs_head;
-            if (p.scale_kind == PA_SCALE_PER_CHANNEL)
-              vs = __bfloat162float(sc_smem ? vs_s[m.kvh * kWDim + dim]
-                                            : reinterpret_cast<const __nv_bfloat16*>(p.v_scale)[m.kvh * kWDim + dim]);
-            const float f = o[j][d][2 * h + e] * inv * vs;
-            if (m.nch == 1) {
-              const int64_t oi = ((int64_t)token * p.q_heads + head) * kWDim + dim;
-              const float fe = ep_value(p.ep, f, head * kWDim + dim);
-              if (p.ep.int8_out)
-                reinterpret_cast<int8_t*>(p.out)[oi] = (int8_t)ep_int8(p.ep, fe);
-              else
-                p.out[oi] = __float2bfloat16_rn(fe);
-            } else {
-              const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
-              p.part_o[sp * kWDim + dim] = __float2bfloat16_rn(f);
-            }
-          }
-        if (g == 0) {
+          for (int h = 0; h < 2; ++h)
+            stg[r * kWDim + ((16 * d + g + 8 * h) ^ (8 * t))] = o[j][d][2 * h + e] * inv;
+        if (g == 0 && r < n_rows) {
+          const int token = m.tok0 + r / G;
+          const int head = m.kvh * G + r % G;
+          const float ln2 = 0.69314718055994530942f;
+          const float mr = mrow[j][e];   // true running max (log2 units, offset term removed)
           if (m.nch == 1) {
             if (p.lse != nullptr)
               p.lse[(int64_t)token * p.q_heads + head] = l > 0.f ? (mr + __log2f(l)) * ln2 : -INFINITY;
@@ -581,7 +624,77 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
         }
       }
     }
+    __syncwarp();
+    {
+      const bool final_row = m.nch == 1;
+      const bool per_channel = p.scale_kind == PA_SCALE_PER_CHANNEL;
+      const float vs_head = p.scale_kind == PA_SCALE_GLOBAL ? reinterpret_cast<const float*>(p.v_scale)[0]
+                            : p.scale_kind == PA_SCALE_PER_KV_HEAD
+                                ? __bfloat162float(sc_smem ? vs_s[m.kvh]
+                                                           : reinterpret_cast<const __nv_bfloat16*>(p.v_scale)[m.kvh])
+                                : 1.f;
+      // 16-byte stores need an aligned out (partial rows always are)
+      const bool vec = !final_row || (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
+#pragma unroll 1
+      for (int idx = lane; idx < n_rows * 16; idx += 32) {
+        const int r = idx >> 4, c = idx & 15;   // row r, dims 8c .. 8c+7
+        const float* src = stg + r * kWDim + ((8 * c) ^ (8 * ((r >> 1) & 3)));
+        const float4 a = *reinterpret_cast<const float4*>(src);
+        const float4 b = *reinterpret_cast<const float4*>(src + 4);
+        float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        if (per_channel) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            v[k] *= __bfloat162float(sc_smem ? vs_s[m.kvh * kWDim + 8 * c + k]
+                                             : reinterpret_cast<const __nv_bfloat16*>(p.v_scale)[m.kvh * kWDim + 8 * c + k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v[k] *= vs_head;
+        }
+        const int token = m.tok0 + r / G;
+        const int head = m.kvh * G + r % G;
+        if (final_row) {
+          const int64_t oi = ((int64_t)token * p.q_heads + head) * kWDim + 8 * c;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v[k] = ep_value(p.ep, v[k], head * kWDim + 8 * c + k);
+          if (p.ep.int8_out) {
+            uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              w0 |= ep_int8(p.ep, v[k]) << (8 * k);
+              w1 |= ep_int8(p.ep, v[4 + k]) << (8 * k);
+            }
+            int8_t* dst = reinterpret_cast<int8_t*>(p.out) + oi;
+            if (vec) {
+              *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) dst[k] = (int8_t)(((k < 4 ? w0 : w1) >> (8 * (k & 3))) & 0xFF);
+            }
+          } else {
+            uint32_t w[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) w[k] = pack_bf162(v[2 * k], v[2 * k + 1]);
+            __nv_bfloat16* dst = p.out + oi;
+            if (vec) {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) dst[k] = __float2bfloat16_rn(v[k]);
+            }
+          }
+        } else {
+          const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
+          uint32_t w[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) w[k] = pack_bf162(v[2 * k], v[2 * k + 1]);
+          *reinterpret_cast<uint4*>(p.part_o + sp * kWDim + 8 * c) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    __syncwarp();   // the staged rows are read before the stage is refilled
     ++k_comp;
+    issue_next();   // the stage of the item's last half page
   }
 
   if (fail || *abort_any) {

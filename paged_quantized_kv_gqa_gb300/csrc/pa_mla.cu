@@ -85,16 +85,18 @@ struct Smem {
 
 // fp16 block kb (dims 64 kb .. 64 kb + 63) of a page from its raw TMA boxes:
 // block kb = the (kb & 1) half of raw box kb >> 1.  Thread t converts row
-// t >> 1, raw chunks 2 (t & 1) .. +1 of that half; rows >= nvalid become zero.
+// t & 63, raw chunks 2 (t >> 6) .. +1 of that half; rows >= nvalid become
+// zero.  Eight neighbouring threads take eight rows, so every 16-byte load
+// and store phase covers all 32 banks.
 template <int FP8>
 __device__ __forceinline__ void convert_block(uint32_t raw, uint32_t dst, int kb, int t,
                                               int nvalid) {
-  const int row = t >> 1;
+  const int row = t & 63;
   const uint32_t src = raw + (kb >> 1) * kBox + row * 128;
   const uint32_t out = dst + kb * kBlk + row * 128;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    const int c = 4 * (kb & 1) + 2 * (t & 1) + h;     // raw 16-byte chunk (16 values)
+    const int c = 4 * (kb & 1) + 2 * (t >> 6) + h;    // raw 16-byte chunk (16 values)
     uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
     if (row < nvalid) {
       const uint4 r4 = ld_shared_v4(src + ((c ^ (row & 7)) << 4));
