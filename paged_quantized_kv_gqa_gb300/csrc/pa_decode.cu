@@ -69,8 +69,18 @@ constexpr int kPBufs = 4;                        // P^T ring depth
 // 128-byte swizzle; a thread (= position) writes its rows with 16-byte stores
 constexpr int kPBufBytes = kTileTok * 128;
 constexpr int kMergeRows = 2;                    // rows a merge warp combines at once
+// Item records and per-kv-head scales kept in shared memory: every role reads
+// them at each item boundary, where a read from memory would wait behind the
+// kernel's own page stream.
+constexpr int kCachedItems = 160;
+constexpr int kCachedHeads = 64;
 
 // The decode pipeline is latency-bound: its waits re-probe every 32 ns.
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
                                       volatile int* abort_any) {
   return wait_or_abort(bar, parity, limit_ns, abort_any, 32);
@@ -100,27 +110,45 @@ struct Smem {
   static constexpr int kNumBars = 2 * kStages + 2 + 2 + 2 + kPBufs + 2 + kPBufs;
   static constexpr int kMisc = kBars + kNumBars * 8;       // tmem addr, abort flags
   static constexpr int kEpDone = kMisc + 32;               // [8] items finished per softmax warp
-  static constexpr int kTotal = kEpDone + 32 + 1024;       // + alignment slack
+  static constexpr int kItems = kEpDone + 32;              // [kCachedItems][8] int32
+  static constexpr int kScales = kItems + kCachedItems * kItemWords * 4;   // k, v [kCachedHeads] fp32
+  static constexpr int kTotal = kScales + 2 * kCachedHeads * 4 + 1024;     // + alignment slack
+  static_assert(kItems % 16 == 0, "item records are read as int4");
   static_assert(kTotal <= 232448, "shared memory overflow");
+};
+
+// The CTA's item records: the first kCachedItems from shared memory.
+struct ItemSrc {
+  const int32_t* cached;   // shared memory
+  const int32_t* items;    // global
+  int begin, n_cached;
+  __device__ __forceinline__ Item at(int it) const {
+    const int k = it - begin;
+    if (k < n_cached) {
+      const int4* r = reinterpret_cast<const int4*>(cached + k * kItemWords);
+      return item_from<kTileTok>(r[0], r[1]);
+    }
+    return load_item<kTileTok>(items, it);
+  }
 };
 
 // Walks the (item, tile) sequence of one CTA.
 struct TileCursor {
   int it, end, i, ntiles;
-  const int32_t* items;
-  __device__ __forceinline__ void init(const int32_t* its, int begin, int e) {
-    items = its;
+  ItemSrc src;
+  __device__ __forceinline__ void init(const ItemSrc& s, int begin, int e) {
+    src = s;
     it = begin;
     end = e;
     i = 0;
-    ntiles = it < end ? load_item<kTileTok>(items, it).ntiles : 0;
+    ntiles = it < end ? src.at(it).ntiles : 0;
   }
   __device__ __forceinline__ bool valid() const { return it < end; }
   __device__ __forceinline__ void advance() {
     if (++i >= ntiles) {
       ++it;
       i = 0;
-      ntiles = it < end ? load_item<kTileTok>(items, it).ntiles : 0;
+      ntiles = it < end ? src.at(it).ntiles : 0;
     }
   }
 };
@@ -190,6 +218,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = 0; w < 8; ++w) ep_done[w] = 0;
     fence_mbar_init();
   }
+  int32_t* items_s = reinterpret_cast<int32_t*>(smem + SM::kItems);
+  float* ks_s = reinterpret_cast<float*>(smem + SM::kScales);
+  float* vs_s = ks_s + kCachedHeads;
+  const ItemSrc isrc{items_s, p.items, item_begin, min(item_end - item_begin, kCachedItems)};
+  for (int i = tid; i < isrc.n_cached * kItemWords; i += kThreads)
+    items_s[i] = p.items[(int64_t)item_begin * kItemWords + i];
+  // per-kv-head or global scales (per-channel ones are read per item)
+  const bool sc_cached = p.scale_kind != PA_SCALE_PER_CHANNEL && p.kv_heads <= kCachedHeads;
+  if (sc_cached)
+    for (int h = tid; h < p.kv_heads; h += kThreads) {
+      ks_s[h] = load_scale(p.k_scale, p.scale_kind, h);
+      vs_s[h] = load_scale(p.v_scale, p.scale_kind, h);
+    }
+  auto kscale = [&](int kvh) { return sc_cached ? ks_s[kvh] : load_scale(p.k_scale, p.scale_kind, kvh); };
+  auto vscale = [&](int kvh) { return sc_cached ? vs_s[kvh] : load_scale(p.v_scale, p.scale_kind, kvh); };
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -208,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued_g[s] = -1;
       bool ok = true;
       for (int it = item_begin; it < item_end && ok; ++it) {
-        const Item m = load_item<kTileTok>(p.items, it);
+        const Item m = isrc.at(it);
         const int32_t* bt = p.block_table + (int64_t)m.b * p.max_blocks;
         for (int t = 0; t < m.ntiles; ++t, ++g) {
           const int stage = g % kStages;
@@ -257,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = idesc_f16_f32(128, NR);
       const uint32_t idesc_pv = idesc_f16_f32_bmn(128, NR);   // B = P^T, MN-major
       TileCursor cs, cp;       // next S to issue, next PV to issue
-      cs.init(p.items, item_begin, item_end);
-      cp.init(p.items, item_begin, item_end);
+      cs.init(isrc, item_begin, item_end);
+      cp.init(isrc, item_begin, item_end);
       uint32_t gs = 0, gp = 0;
       uint32_t s_commits[2] = {0, 0}, pv_commits[kPBufs] = {0, 0, 0, 0};
       bool ok = true;
@@ -345,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         __threadfence_block();   // acquire the epilogue's partial-state writes
-        const Item m = load_item<kTileTok>(p.items, it);
+        const Item m = isrc.at(it);
         if (m.nch <= 1) continue;
         int32_t* cnt = p.merge_cnt + (int64_t)m.tok0 * p.kv_heads + m.kvh;
         int prev = 0;
@@ -405,13 +448,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // O^T row d = this thread's TMEM lane, times 1/l and the V scale
     auto epilogue = [&](int li, uint32_t gl) -> bool {
       const int it = item_begin + li;
-      const Item m = load_item<kTileTok>(p.items, it);
-      if (!dwait(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) {
-        note_fail(it);
-        return false;
-      }
+      const Item m = isrc.at(it);
+      // a failed wait is published through the warpgroup's abort flag and
+      // acted on after the named barrier below, so that every thread of the
+      // warpgroup reaches that barrier
+      if (!fail && !dwait(&pvdone[gl & 3], (gl >> 2) & 1, limit, abort_any)) note_fail(it);
       tc_fence_after();
+      // O^T columns (thread = head dim d) are staged as fp32 [j][d], 16 rows
+      // per pass, in the P^T slot of tile gl: PV_gl has completed, and that
+      // slot is written again only for tile gl + 4, whose S needs both
+      // warpgroups to have read S of tile gl + 2, i.e. to be past this
+      // epilogue.  Warpgroup wg uses bytes [8 KB wg, 8 KB wg + 8 KB).  The rows
+      // then leave as 16-byte pieces from a rolled loop that applies 1/l, the
+      // V scale and the output epilogue: this code runs at about the same
+      // moment in every CTA and is kept small.
       const int d = pos_in_tile;
+      const int n_rows = m.ntok * G;
+      float* stg = reinterpret_cast<float*>(smem + SM::kP + (gl & 3) * kPBufBytes + wg * 8192);
+      const float* inv = lsum_s + (li & 1) * NR;
+      const bool per_channel = p.scale_kind == PA_SCALE_PER_CHANNEL;
+      const float vs_head = per_channel ? 1.0f : vscale(m.kvh);
+      const bool vec = m.nch > 1 || (reinterpret_cast<uintptr_t>(p.out) & 15) == 0;
       uint32_t v[NH];
 #pragma unroll
       for (int c = 0; c < NH / 8; ++c)
@@ -419,32 +476,68 @@ __global__ void __launch_bounds__(kThreads, 1)
                  *reinterpret_cast<uint32_t(*)[8]>(&v[8 * c]));
       tmem_wait_ld();
       tc_fence_before();
-      const float vs = load_scale(p.v_scale, p.scale_kind,
-                                  p.scale_kind == PA_SCALE_PER_CHANNEL ? m.kvh * kHeadDim + d : m.kvh);
-      const float* inv = lsum_s + (li & 1) * NR;
-      const int n_rows = m.ntok * G;
-      int token = m.tok0 + r_lo / G, gq = r_lo % G;   // row r_lo + j <-> (token, gq)
+      // rows j0 .. j0 + nj - 1 of this warpgroup, from the staging buffer
+      auto write_rows = [&](int j0, int nj) {
+#pragma unroll 1
+        for (int q = pos_in_tile; q < nj * 16; q += 128) {
+          const int j = q >> 4, c = q & 15;   // row r_lo + j0 + j, dims 8c .. 8c+7
+          const int r = r_lo + j0 + j;
+          if (r >= n_rows) continue;
+          const float4 a = *reinterpret_cast<const float4*>(stg + j * kHeadDim + 8 * c);
+          const float4 b = *reinterpret_cast<const float4*>(stg + j * kHeadDim + 8 * c + 4);
+          float f[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+          const float sc = inv[r] * vs_head;
 #pragma unroll
-      for (int j = 0; j < NH; ++j) {
-        if (r_lo + j < n_rows) {
-          const int head = m.kvh * G + gq;
-          const float f = __uint_as_float(v[j]) * inv[r_lo + j] * vs;
+          for (int k = 0; k < 8; ++k)
+            f[k] *= per_channel ? sc * load_scale(p.v_scale, p.scale_kind, m.kvh * kHeadDim + 8 * c + k) : sc;
+          const int token = m.tok0 + r / G;
+          const int head = m.kvh * G + r % G;
           if (m.nch == 1) {
-            const int64_t o = ((int64_t)token * p.q_heads + head) * kHeadDim + d;
-            const float fe = ep_value(p.ep, f, head * kHeadDim + d);
-            if (p.ep.int8_out)
-              reinterpret_cast<int8_t*>(p.out)[o] = (int8_t)ep_int8(p.ep, fe);
-            else
-              p.out[o] = __float2bfloat16_rn(fe);
+            const int64_t o = ((int64_t)token * p.q_heads + head) * kHeadDim + 8 * c;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = ep_value(p.ep, f[k], head * kHeadDim + 8 * c + k);
+            if (p.ep.int8_out) {
+              int8_t* dst = reinterpret_cast<int8_t*>(p.out) + o;
+              if (vec) {
+                uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  w0 |= ep_int8(p.ep, f[k]) << (8 * k);
+                  w1 |= ep_int8(p.ep, f[4 + k]) << (8 * k);
+                }
+                *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+              } else {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) dst[k] = (int8_t)ep_int8(p.ep, f[k]);
+              }
+            } else if (vec) {
+              *reinterpret_cast<uint4*>(p.out + o) =
+                  make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                             pack_bf16x2(f[6], f[7]));
+            } else {
+#pragma unroll
+              for (int k = 0; k < 8; ++k) p.out[o + k] = __float2bfloat16_rn(f[k]);
+            }
           } else {
             const int64_t sp = ((int64_t)token * p.max_chunks + m.chunk) * p.q_heads + head;
-            p.part_o[sp * kHeadDim + d] = __float2bfloat16_rn(f);
+            *reinterpret_cast<uint4*>(p.part_o + sp * kHeadDim + 8 * c) =
+                make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                           pack_bf16x2(f[6], f[7]));
           }
         }
-        if (++gq == G) {
-          gq = 0;
-          ++token;
-        }
+      };
+      constexpr int kP0 = NH < 16 ? NH : 16;   // rows of the first pass
+#pragma unroll
+      for (int j = 0; j < kP0; ++j) stg[j * kHeadDim + d] = __uint_as_float(v[j]);
+      bar_sync(bar_id, 128);
+      if (*my_abort) return false;
+      write_rows(0, kP0);
+      if constexpr (NH > kP0) {
+        bar_sync(bar_id, 128);   // the first pass has read the staging buffer
+#pragma unroll
+        for (int j = kP0; j < NH; ++j) stg[(j - kP0) * kHeadDim + d] = __uint_as_float(v[j]);
+        bar_sync(bar_id, 128);
+        write_rows(kP0, NH - kP0);
       }
       if (p.merge_cnt != nullptr) {
         // publish: this warp's rows of item li are written (release to the merge warps)
@@ -462,11 +555,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t g = 0;
     float l[NH];
     for (int it = item_begin; it < item_end && !stop; ++it) {
-      const Item cur = load_item<kTileTok>(p.items, it);
+      const Item cur = isrc.at(it);
       const int li = it - item_begin;
       const int n_rows = cur.ntok * G;
       const float c_log2 = p.sm_scale_log2 *
-          (p.scale_kind == PA_SCALE_PER_CHANNEL ? 1.0f : load_scale(p.k_scale, p.scale_kind, cur.kvh));
+          (p.scale_kind == PA_SCALE_PER_CHANNEL ? 1.0f : kscale(cur.kvh));
       const uint32_t o_col = TM::O0 + (li & 1) * NR + r_lo;
       // speculative tree mask: the item's first token within its sequence and
       // the sequence's cached prefix length (appended positions start there)
@@ -744,8 +837,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
     };
+    int q_ahead = -1;   // item whose Q' was written during the previous item
     for (int it = item_begin; it < item_end && !fail; ++it) {
-      const Item m = load_item<kTileTok>(p.items, it);
+      const Item m = isrc.at(it);
       const int li = it - item_begin;
       for (int i = 0; i < m.ntiles; ++i, ++g) {
         const int stage = g % kStages;
@@ -755,7 +849,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           note_fail(it);
           break;
         }
-        if (i == 0) load_q(m, q_s + (li & 1) * NR * 256);
+        if (i == 0) {
+          if (q_ahead != it) load_q(m, q_s + (li & 1) * NR * 256);
+          // the next item's query rows into L2 now; its Q' is written at this
+          // item's second tile (below), so that no item boundary waits for it
+          if (it + 1 < item_end) {
+            const Item mn = isrc.at(it + 1);
+            const int rows = mn.ntok * G;
+            if (d < 2 * rows) {
+              const int r = d >> 1;
+              prefetch_l2(p.q + (int64_t)(mn.tok0 + r / G) * p.q_stride + (mn.kvh * G + r % G) * kHeadDim +
+                          64 * (d & 1));
+            }
+          }
+        }
+        if (i == 1 && it + 1 < item_end) {
+          // Q' buffer (li + 1) & 1 was last read by the S of item li - 1, whose
+          // last tile is g - 2 or earlier
+          load_q(isrc.at(it + 1), q_s + ((li + 1) & 1) * NR * 256);
+          q_ahead = it + 1;
+        }
         if (!wait_or_abort(&full[stage], (g / kStages) & 1, limit, abort_any)) { note_fail(it); break; }
         if (d == 0) trace_ev(p, g, 1);
         {
