@@ -404,6 +404,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int i = 0; i < m.ntiles; ++i, ++g) {
         const int stage = (int)(g % (uint32_t)stages);
         const uint32_t raw = raw0 + stage * stage_bytes;
+        if (q_loader && i == max(0, m.ntiles - 8) && it + 1 < item_end) {
+          // the next item's query rows (this thread's head: 1152 bytes, nine
+          // 128-byte lines) into L2 a few pages ahead, so that loading them at
+          // the item boundary does not wait for memory
+          const __nv_bfloat16* nq = p.q + (int64_t)load_item<kTile>(p.items, it + 1).tok0 * p.q_stride +
+                                    (int64_t)t * kDqk;
+#pragma unroll
+          for (int k = 0; k < 9; ++k) prefetch_l2(nq + 64 * k);
+        }
         const int nvalid = min(kTile, m.kv1 - (m.kv0 + i * kTile));
         if (!wait_or_abort(&full[stage], (g / (uint32_t)stages) & 1, limit, abort_any)) {
           fail = true;
