@@ -105,14 +105,14 @@ def _peaks(bound: str):
 # while the kernel's sources still hash to the version it was taken with.
 NCU_TRAFFIC = {
     # decode-2 runs the warp-per-item kernel (at most 16 packed rows)
-    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "cdb7c2ddca799532", 318.229504e6 + 4.232960e6),
+    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "331e64000ff7af0d", 318.199808e6 + 4.275712e6),
     # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
     # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
     # states written both grow per sequence
-    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "49ea2af2be92949e",
-                      (729.503232e6 + 31.330304e6) * 7.492152264116904),
-    "append-3": (("pa_append.cu",), "b20bc32183b1cbe9", 72.253952e6 + 2.531840e6),
-    "mla-5": (("pa_mla.cu",), "42e261b723a89932", 199.476992e6 + 23.214592e6),
+    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "4acba54fe57c746b",
+                      (729.476352e6 + 31.757312e6) * 7.492152264116904),
+    "append-3": (("pa_append.cu",), "bbe9ab1be6b9dd29", 72.232704e6 + 1.659136e6),
+    "mla-5": (("pa_mla.cu",), "c33e804c034ae660", 199.417600e6 + 23.168768e6),
 }
 
 

@@ -318,7 +318,8 @@ pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load);
  * 4 P ready, 5/6 V dequantisation start/end, 7 V ready, 8 score MMA issued,
  * 9 PV MMA issued, 10 item epilogue done, 11 P buffer free.  Warp-per-item
  * decode kernel (tile = the warp's n-th half page): event w = warp w finished
- * it, 12 + w = it had landed (warps 0..3).  NULL disables tracing.
+ * it, 12 + w = warp w found it landed (passed its wait; warps 0..3).  NULL
+ * disables tracing.  paged_quantized_kv_gqa_gb300/trace.py prints a summary.
  * Process-wide setting.
  */
 pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta);
