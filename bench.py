@@ -85,6 +85,11 @@ HEADLINE = 2
 ALL_WORKLOADS = (2, 1, 4, 3, 5)       # headline first
 
 
+# GB300 nominal peaks, reported beside the measured ones: HBM3e 7.9 TB/s,
+# dense bf16 / fp16 tensor 2.25 PFLOP/s
+NOMINAL_PEAK = {"hbm": 7900.0, "tensor": 2250.0}
+
+
 def _peaks(bound: str):
     """(peak, source) for an HBM-bound (GB/s) or tensor-bound (TFLOP/s) kernel.
     The fp16 kind::f16 tensor rate equals the bf16 one the peaks file measures;
@@ -100,9 +105,9 @@ def _peaks(bound: str):
 
 
 # DRAM bytes (read + written) per launch of each attention kernel, from one
-# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on the workload
-# (the kept ncu traffic summary under profiles/).  A figure is reported only
-# while the kernel's sources still hash to the version it was taken with.
+# ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on the workload.
+# A figure is reported only while the kernel's sources still hash to the
+# version it was taken with.
 NCU_TRAFFIC = {
     # decode-2 runs the warp-per-item kernel (at most 16 packed rows)
     "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "331e64000ff7af0d", 318.199808e6 + 4.275712e6),
@@ -512,7 +517,9 @@ def run_workload(cfg: int, case, args, world: int, local: int, dev, pool) -> dic
             "frac": round(achieved / peak, 4), "traffic": _traffic(case.name),
             "traffic_unit": "bytes per launch (ncu)", "peak_source": peak_kind + " (of measured)"
             if peak_kind.startswith("measured") else peak_kind,
-            "kernel": "pa_run attention kernel", "run_ms": round(run_mean, 5)}
+            "kernel": "pa_run attention kernel", "run_ms": round(run_mean, 5),
+            "nominal_peak": NOMINAL_PEAK[bound],
+            "frac_of_nominal": round(achieved / NOMINAL_PEAK[bound], 4)}
     if kind == "latency":
         # two short sequences: the step is bound by launch latency, so it is
         # reported as a latency; the byte rate is shown for reference only
