@@ -76,6 +76,25 @@ def test_decode_edge_cases(kw):
     compare(case, out, lse, label=str(kw))
 
 
+@pytest.mark.parametrize("kw", [
+    # at most 16 packed rows per tile (warp-per-item kernel), one chunk
+    dict(seq_lens=[1, 1], seq_lens_kv=[300, 70], q_heads=8, kv_heads=2, chunk_size=0),
+    # 48 packed rows per tile (tensor-memory kernel), one chunk
+    dict(seq_lens=[6], seq_lens_kv=[700], q_heads=64, kv_heads=8, chunk_size=0),
+])
+def test_decode_unaligned_out(kw):
+    """The decode family takes an out that is not 16-byte aligned: its kernels
+    write whole rows with 16-byte stores only when out allows them."""
+    case = synth.make_case(name="unaligned out", seed=11, **kw)
+    d = to_device(case)
+    flat = torch.zeros(d["out"].numel() + 1, dtype=d["out"].dtype, device=d["out"].device)
+    d["out"] = flat[1:].view(d["out"].shape)          # 2 bytes past a 16-byte boundary
+    assert d["out"].data_ptr() % 16 != 0
+    out, lse, plan, _, _ = run_case(case, d=d)
+    assert plan.describe()["family"] == "decode"
+    compare(case, out, lse, label="unaligned out " + str(kw))
+
+
 def test_page_permutation_invariance_bitexact():
     """Same logical cache under two physical page permutations: identical output bits."""
     a = synth.make_case(name="perm", seed=9, seq_lens=[1, 3, 2], seq_lens_kv=[700, 1500, 64],
