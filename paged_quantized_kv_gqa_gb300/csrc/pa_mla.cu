@@ -53,6 +53,11 @@ constexpr int kPBytes = kRows * 128;             // P tile: 128 rows x 64 fp16
 constexpr int kMetaBytes = 1040;                 // alpha[128], inv_l[128], flag, last
 constexpr int kPXfer = kPBytes + kMetaBytes;     // bytes shipped per tile
 constexpr int kPBuf = 18432;                     // P buffer stride (1024-aligned)
+// P tiles in flight between the two CTAs: the score CTA writes P of page g
+// once the value CTA's PV of page g - kPRing has completed, so the loop
+// softmax -> copy -> correction -> PV -> completion relay spans kPRing pages
+// (three measured no faster than two on the MLA workload)
+constexpr int kPRing = 2;
 constexpr int kStages0 = 2;                      // raw K page ring (score CTA)
 constexpr int kStages1 = 3;                      // raw V page ring (value CTA)
 constexpr float kTau = 8.0f;
@@ -72,12 +77,12 @@ struct Smem {
   static constexpr int kRaw1 = 0;
   static constexpr int kV16 = kRaw1 + kStages1 * kVBoxes * kBox;   // 98304
   static constexpr int kPin = kV16 + kVBlocks * kBlk;              // 163840
-  static constexpr int kEnd = kPin + 2 * kPBuf;                    // 200704
-  static_assert(kPout + 2 * kPBuf <= kEnd, "layout");
+  static constexpr int kEnd = kPin + kPRing * kPBuf;                // 200704
+  static_assert(kPout + kPRing * kPBuf <= kEnd, "layout");
   static constexpr int kBars = kEnd;
-  // full[3] empty[3] kready[3] kfree[3] sfull[2] sfree[2] qready qfree pvfree[2]
-  // pfull[2] corr[2] vready[2] vfree[2] pvdone[2] drain
-  static constexpr int kNumBars = 3 + 3 + 3 + 3 + 2 + 2 + 1 + 1 + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+  // full[3] empty[3] kready[3] kfree[3] sfull[2] sfree[2] qready qfree pvfree[R]
+  // pfull[R] corr[R] vready[2] vfree[2] pvdone[R] drain  (R = kPRing)
+  static constexpr int kNumBars = 3 + 3 + 3 + 3 + 2 + 2 + 1 + 1 + 4 * kPRing + 2 + 2 + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16 + 1024;
   static_assert(kTotal <= 232448, "shared memory overflow");
@@ -129,13 +134,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* sfree = sfull + 2;      // [2]
   uint64_t* qready = sfree + 2;
   uint64_t* qfree = qready + 1;
-  uint64_t* pvfree = qfree + 1;     // [2] (score CTA, arrived on by the value CTA)
-  uint64_t* pfull = pvfree + 2;     // [2] (value CTA, completed by the score CTA's copies)
-  uint64_t* corr = pfull + 2;       // [2]
-  uint64_t* vready = corr + 2;      // [2]
+  uint64_t* pvfree = qfree + 1;     // [kPRing] (score CTA, arrived on by the value CTA)
+  uint64_t* pfull = pvfree + kPRing;   // [kPRing] (value CTA, completed by the score CTA's copies)
+  uint64_t* corr = pfull + kPRing;  // [kPRing]
+  uint64_t* vready = corr + kPRing; // [2]
   uint64_t* vfree = vready + 2;     // [2]
-  uint64_t* pvdone = vfree + 2;     // [2]
-  uint64_t* drain = pvdone + 2;
+  uint64_t* pvdone = vfree + 2;     // [kPRing]
+  uint64_t* drain = pvdone + kPRing;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
   volatile int* abort_any = reinterpret_cast<volatile int*>(smem + SM::kMisc + 4);
   volatile int* abort_sm = reinterpret_cast<volatile int*>(smem + SM::kMisc + 8);  // softmax group
@@ -164,10 +169,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int j = 0; j < 2; ++j) {
       mbar_init(&sfull[j], 1);
       mbar_init(&sfree[j], 4);
-      mbar_init(&pvfree[j], 1);
-      mbar_init(&pfull[j], 1);
       mbar_init(&vready[j], 4);
       mbar_init(&vfree[j], 1);
+    }
+    for (int j = 0; j < kPRing; ++j) {
+      mbar_init(&pvfree[j], 1);
+      mbar_init(&pfull[j], 1);
       mbar_init(&pvdone[j], 1);
       mbar_init(&corr[j], 4);
     }
@@ -177,10 +184,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     *abort_any = 0;
     *abort_sm = 0;
     fence_mbar_init();
-    if (rank == 1) {   // expect the first two P tiles
-      mbar_arrive_expect_tx(&pfull[0], kPXfer);
-      mbar_arrive_expect_tx(&pfull[1], kPXfer);
-    }
+    if (rank == 1)     // expect the first kPRing P tiles
+      for (int j = 0; j < kPRing; ++j) mbar_arrive_expect_tx(&pfull[j], kPXfer);
   }
   if (warp == 0) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
@@ -298,10 +303,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int it = item_begin; it < item_end && ok; ++it) {
         const Item m = load_item<kTile>(p.items, it);
         for (int i = 0; i < m.ntiles; ++i, ++g) {
-          if (!wait_or_abort(&pfull[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
-          if (lane == 0) mbar_arrive_expect_tx(&pfull[g & 1], kPXfer);   // P tile two steps ahead
-          if (!wait_or_abort(&corr[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
-          const uint32_t pa_ = pin + (g & 1) * kPBuf;
+          const int pr = (int)(g % kPRing);
+          const uint32_t ph = (g / kPRing) & 1;
+          if (!wait_or_abort(&pfull[pr], ph, limit, abort_any)) { ok = false; break; }
+          if (lane == 0) mbar_arrive_expect_tx(&pfull[pr], kPXfer);   // P tile kPRing steps ahead
+          if (!wait_or_abort(&corr[pr], ph, limit, abort_any)) { ok = false; break; }
+          const uint32_t pa_ = pin + pr * kPBuf;
           for (int hv = 0; hv < 2 && ok; ++hv) {
             if (!wait_or_abort(&vready[hv], g & 1, limit, abort_any)) { ok = false; break; }
             tc_fence_after();
@@ -316,7 +323,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
           }
           if (!ok) break;
-          if (elect_one()) tc_commit(&pvdone[g & 1]);
+          if (elect_one()) tc_commit(&pvdone[pr]);
           __syncwarp();
           if (lane == 0) trace_ev(p, g, 11);
         }
@@ -329,15 +336,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (rank == 1 && warp == kWarpRelay) {
     // ================================================================ PV done -> score CTA
     if (lane == 0) {
-      const uint32_t rem0 = mapa_shared(smem_u32(&pvfree[0]), peer);
-      const uint32_t rem1 = mapa_shared(smem_u32(&pvfree[1]), peer);
+      const uint32_t rem0 = mapa_shared(smem_u32(&pvfree[0]), peer);   // pvfree[j] at rem0 + 8 j
       uint32_t g = 0;
       for (int it = item_begin; it < item_end; ++it) {
         const Item m = load_item<kTile>(p.items, it);
         bool ok = true;
         for (int i = 0; i < m.ntiles; ++i, ++g) {
-          if (!wait_or_abort(&pvdone[g & 1], (g >> 1) & 1, limit, abort_any)) { ok = false; break; }
-          mbar_arrive_remote((g & 1) ? rem1 : rem0);
+          if (!wait_or_abort(&pvdone[g % kPRing], (g / kPRing) & 1, limit, abort_any)) { ok = false; break; }
+          mbar_arrive_remote(rem0 + 8 * (g % kPRing));
         }
         if (!ok) break;
       }
@@ -437,8 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int h = tid & 127;
     const uint32_t pout = s_base + SM::kPout;
     const uint32_t pin_peer = mapa_shared(s_base + SM::kPin, peer);
-    const uint32_t pfull_peer0 = mapa_shared(smem_u32(&pfull[0]), peer);
-    const uint32_t pfull_peer1 = mapa_shared(smem_u32(&pfull[1]), peer);
+    const uint32_t pfull_peer0 = mapa_shared(smem_u32(&pfull[0]), peer);   // pfull[j] at + 8 j
     const float c_log2 = p.sm_scale_log2 * gscale;
     uint32_t g = 0;
     bool fail = false;
@@ -482,10 +487,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const bool flag = bar_or(1, 128, need && i > 0);
         if (*abort_sm) { fail = true; break; }
         const float neg_m = m_run == -INFINITY ? 0.0f : -m_run;
-        // local P buffer g&1 (and the peer's) are free once PV of tile g-2 completed
-        if (g >= 2 && !wait_or_abort(&pvfree[g & 1], ((g - 2) >> 1) & 1, limit, abort_any))
+        // local P buffer g % R (and the peer's) are free once PV of tile g - R
+        // completed (R = kPRing; its copy had completed before that PV began)
+        const int pr = (int)(g % kPRing);
+        if (g >= (uint32_t)kPRing &&
+            !wait_or_abort(&pvfree[pr], ((g - kPRing) / kPRing) & 1, limit, abort_any))
           *abort_sm = 1;
-        const uint32_t buf = pout + (g & 1) * kPBuf;
+        const uint32_t buf = pout + pr * kPBuf;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint32_t w[16];
@@ -506,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]));
           }
         }
-        float* meta = reinterpret_cast<float*>(smem + SM::kPout + (g & 1) * kPBuf + kPBytes);
+        float* meta = reinterpret_cast<float*>(smem + SM::kPout + pr * kPBuf + kPBytes);
         const bool last = i + 1 == m.ntiles;
         meta[h] = alpha;
         if (last) meta[kRows + h] = l > 0.0f ? __frcp_rn(l) : 0.0f;
@@ -530,7 +538,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bar_sync(1, 128);
         if (*abort_sm) { fail = true; break; }
         if (h == 0) {
-          bulk_s2peer(pin_peer + (g & 1) * kPBuf, buf, kPXfer, (g & 1) ? pfull_peer1 : pfull_peer0);
+          bulk_s2peer(pin_peer + pr * kPBuf, buf, kPXfer, pfull_peer0 + 8 * pr);
           trace_ev(p, g, 8);
         }
       }
@@ -545,17 +553,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int it = item_begin; it < item_end && !fail; ++it) {
       const Item m = load_item<kTile>(p.items, it);
       for (int i = 0; i < m.ntiles; ++i, ++g) {
-        if (!wait_or_abort(&pfull[g & 1], (g >> 1) & 1, limit, abort_any)) { fail = true; break; }
+        const int pr = (int)(g % kPRing);
+        if (!wait_or_abort(&pfull[pr], (g / kPRing) & 1, limit, abort_any)) { fail = true; break; }
         if (h == 0) trace_ev(p, g, 9);
         const float* meta =
-            reinterpret_cast<const float*>(smem + SM::kPin + (g & 1) * kPBuf + kPBytes);
+            reinterpret_cast<const float*>(smem + SM::kPin + pr * kPBuf + kPBytes);
         const float alpha = meta[h];
         const bool flag = reinterpret_cast<const int*>(meta)[2 * kRows] != 0;
         const bool last = i + 1 == m.ntiles;
         const float inv_l = last ? meta[kRows + h] : 0.0f;
         if (flag) {
           // O holds the PV of earlier tiles of this item: wait for the last one
-          if (!wait_or_abort(&pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1, limit, abort_any)) {
+          if (!wait_or_abort(&pvdone[(g - 1) % kPRing], ((g - 1) / kPRing) & 1, limit, abort_any)) {
             fail = true;
             break;
           }
@@ -572,10 +581,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        warp_arrive(&corr[g & 1], lane);
+        warp_arrive(&corr[pr], lane);
         if (h == 0) trace_ev(p, g, 10);
         if (last) {
-          if (!wait_or_abort(&pvdone[g & 1], (g >> 1) & 1, limit, abort_any)) { fail = true; break; }
+          if (!wait_or_abort(&pvdone[pr], (g / kPRing) & 1, limit, abort_any)) { fail = true; break; }
           tc_fence_after();
           // one chunk: the final row (output epilogue applied); several: the
           // normalised partial row for the merge
