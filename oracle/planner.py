@@ -35,6 +35,17 @@ Spec:
   with work_indptr[num_ctas + 1].
   nch_token[t] = nch of token t's tile; max_chunks = max(1, max nch_token);
   merge_tokens = tokens with nch_token > 1, ascending.
+  MLA with chunk_size = -1 replaces the chunk size and the longest-first
+  deal by contiguous shares (this library's scheduling choice; the pages fix
+  only what an item computes): the tiles' pages, ceil(lim / B) per tile,
+  are numbered consecutively in tile order; quota = max(4, ceil(total /
+  slots)); num_ctas = ceil(total / quota); CTA pair k owns pages [k*quota,
+  min(total, (k+1)*quota)).  For each k, for each tile overlapping that
+  range (tile order), one item covers the overlap: kv0 = (first overlapping
+  page - the tile's first page) * B, kv1 = min(lim, (end of overlap - the
+  tile's first page) * B), chunk index = how many pieces of that tile came
+  before it, nch = the number of pairs overlapping the tile.  chunk (as
+  reported) = quota * B if some tile has nch > 1, else 0.
 """
 from __future__ import annotations
 
@@ -72,6 +83,9 @@ def plan(p, num_sms: int) -> dict:
             tok1 = min(ql, tok0 + tpt)
             lim = slkv[b] + tok1 if p.causal else slkv[b] + ql
             tiles.append((b, tok0, tok1, lim))
+
+    if family == "mla" and int(p.chunk_size) == -1:
+        return _mla_shares(p, tiles, slots, tpt, q_lens, slkv, cu, B)
 
     cs = int(p.chunk_size)
     if cs == -1:
@@ -115,4 +129,41 @@ def plan(p, num_sms: int) -> dict:
     merge_tokens = np.nonzero(nch_token > 1)[0].astype(np.int32)
     return dict(family=family, chunk=cs, tokens_per_tile=tpt, num_ctas=num_ctas,
                 items=arr, work_indptr=indptr, nch_token=nch_token,
+                max_chunks=max_chunks, merge_tokens=merge_tokens)
+
+
+def _mla_shares(p, tiles, slots, tpt, q_lens, slkv, cu, B):
+    """Contiguous shares of all tiles' pages (the MLA rule in the spec above)."""
+    npages = [math.ceil(lim / B) for (_, _, _, lim) in tiles]
+    start = [sum(npages[:i]) for i in range(len(tiles))]       # first page of each tile
+    total = sum(npages)
+    quota = max(4, math.ceil(total / slots))
+    num_ctas = math.ceil(total / quota)
+    owners = [[k for k in range(num_ctas)
+               if start[i] < min(total, (k + 1) * quota) and start[i] + npages[i] > k * quota]
+              for i in range(len(tiles))]
+    T = cu[-1] if cu else 0
+    nch_token = np.zeros(T, dtype=np.int32)
+    for i, (b, tok0, tok1, lim) in enumerate(tiles):
+        nch_token[cu[b] + tok0:cu[b] + tok1] = len(owners[i])
+    rows = []
+    indptr = np.zeros(num_ctas + 1, dtype=np.int32)
+    for k in range(num_ctas):
+        lo, hi = k * quota, min(total, (k + 1) * quota)
+        for i, (b, tok0, tok1, lim) in enumerate(tiles):
+            if k not in owners[i]:
+                continue
+            first = max(lo, start[i]) - start[i]
+            last = min(hi, start[i] + npages[i]) - start[i]
+            base = slkv[b] + tok0 if p.causal else slkv[b] + q_lens[b]
+            c = owners[i].index(k)
+            rows.append((b, 0, cu[b] + tok0, tok1 - tok0, base, first * B, min(lim, last * B),
+                         c | (len(owners[i]) << 16)))
+        indptr[k + 1] = len(rows)
+    arr = np.array(rows, dtype=np.int64).reshape(-1, 8).astype(np.int32)
+    split = bool(T) and int(nch_token.max()) > 1
+    max_chunks = int(max(1, nch_token.max() if T else 1))
+    merge_tokens = np.nonzero(nch_token > 1)[0].astype(np.int32)
+    return dict(family="mla", chunk=quota * B if split else 0, tokens_per_tile=tpt,
+                num_ctas=num_ctas, items=arr, work_indptr=indptr, nch_token=nch_token,
                 max_chunks=max_chunks, merge_tokens=merge_tokens)

@@ -140,69 +140,116 @@ static pa_status build_plan(const pa_problem& prob, const int32_t* ql, const int
       tiles.push_back({b, tok0, tok1, lim});
     }
   }
-  int64_t cs = prob.chunk_size;
-  if (cs == -1) {
-    if (tiles.empty()) {
-      cs = 0;
-    } else {
-      int64_t W = 0, maxlim = 0;
-      for (auto& t : tiles) {
-        W += t.lim;
-        maxlim = std::max(maxlim, t.lim);
-      }
-      W *= prob.kv_heads;
-      const int64_t target = 4LL * slots;
-      cs = std::max<int64_t>(4LL * B, ceil_div(ceil_div(W, target), B) * B);
-      if (cs >= maxlim) cs = 0;
+  if (P.family == PA_FAMILY_MLA && prob.chunk_size == -1) {
+    // MLA with the planner's choice: contiguous shares.  The pages of all
+    // tiles, tile after tile, are cut into shares of `quota` pages; CTA pair k
+    // runs the pieces of the tiles that overlap share k, in tile order.  A
+    // tile's pieces are its chunks (in position order), so a pair loads the
+    // 147 KB query of a token once per piece and every pair gets the same
+    // number of pages (the last one fewer).
+    std::vector<int64_t> first_page(tiles.size() + 1, 0);
+    for (size_t i = 0; i < tiles.size(); ++i)
+      first_page[i + 1] = first_page[i] + ceil_div(tiles[i].lim, (int64_t)B);
+    const int64_t total = first_page.back();
+    const int64_t quota = std::max<int64_t>(4, ceil_div(total, (int64_t)slots));
+    P.num_ctas = (int)ceil_div(total, quota);
+    std::vector<int> nch(tiles.size(), 0);
+    for (int k = 0; k < P.num_ctas; ++k) {
+      const int64_t a = k * quota, e = std::min(total, a + quota);
+      for (size_t i = 0; i < tiles.size(); ++i)
+        if (first_page[i] < e && first_page[i + 1] > a) ++nch[i];
     }
-  }
-  P.chunk = (int32_t)cs;
-  const bool split = cs > 0;
+    P.nch_token.assign(P.total_q, 0);
+    bool any_split = false;
+    for (size_t i = 0; i < tiles.size(); ++i) {
+      if (nch[i] > 0xFFFF) return fail(PA_ERR_UNSUPPORTED, "too many chunks per row");
+      any_split = any_split || nch[i] > 1;
+      for (int tok = tiles[i].tok0; tok < tiles[i].tok1; ++tok) P.nch_token[cu[tiles[i].b] + tok] = nch[i];
+    }
+    P.chunk = any_split ? (int32_t)(quota * B) : 0;
+    std::vector<int> piece(tiles.size(), 0);
+    P.work_indptr.assign(P.num_ctas + 1, 0);
+    P.items.clear();
+    for (int k = 0; k < P.num_ctas; ++k) {
+      const int64_t a = k * quota, e = std::min(total, a + quota);
+      for (size_t i = 0; i < tiles.size(); ++i) {
+        if (!(first_page[i] < e && first_page[i + 1] > a)) continue;
+        const Tile& t = tiles[i];
+        const int64_t kv0 = (std::max(a, first_page[i]) - first_page[i]) * B;
+        const int64_t kv1 = std::min<int64_t>(t.lim, (std::min(e, first_page[i + 1]) - first_page[i]) * B);
+        const int64_t base = prob.causal ? (int64_t)slkv[t.b] + t.tok0 : (int64_t)slkv[t.b] + ql[t.b];
+        const int32_t rec[kItemWords] = {t.b, 0, cu[t.b] + t.tok0, t.tok1 - t.tok0, (int32_t)base,
+                                         (int32_t)kv0, (int32_t)kv1,
+                                         (int32_t)(piece[i]++ | (nch[i] << 16))};
+        P.items.insert(P.items.end(), rec, rec + kItemWords);
+      }
+      P.work_indptr[k + 1] = (int32_t)(P.items.size() / kItemWords);
+    }
+  } else {
+    int64_t cs = prob.chunk_size;
+    if (cs == -1) {
+      if (tiles.empty()) {
+        cs = 0;
+      } else {
+        int64_t W = 0, maxlim = 0;
+        for (auto& t : tiles) {
+          W += t.lim;
+          maxlim = std::max(maxlim, t.lim);
+        }
+        W *= prob.kv_heads;
+        const int64_t target = 4LL * slots;
+        cs = std::max<int64_t>(4LL * B, ceil_div(ceil_div(W, target), B) * B);
+        if (cs >= maxlim) cs = 0;
+      }
+    }
+    P.chunk = (int32_t)cs;
+    const bool split = cs > 0;
 
-  std::vector<int32_t> items;
-  P.nch_token.assign(P.total_q, 0);
-  for (auto& t : tiles) {
-    const int nch = split ? (int)ceil_div(t.lim, cs) : 1;
-    if (nch > 0xFFFF) return fail(PA_ERR_UNSUPPORTED, "too many chunks per row");
-    const int64_t base = prob.causal ? (int64_t)slkv[t.b] + t.tok0 : (int64_t)slkv[t.b] + ql[t.b];
-    for (int tok = t.tok0; tok < t.tok1; ++tok) P.nch_token[cu[t.b] + tok] = nch;
-    for (int kvh = 0; kvh < prob.kv_heads; ++kvh) {
-      for (int c = 0; c < nch; ++c) {
-        const int64_t kv0 = split ? (int64_t)c * cs : 0;
-        const int64_t kv1 = split ? std::min<int64_t>(t.lim, kv0 + cs) : t.lim;
-        const int32_t rec[kItemWords] = {t.b, kvh, cu[t.b] + t.tok0, t.tok1 - t.tok0,
-                                         (int32_t)base, (int32_t)kv0, (int32_t)kv1,
-                                         (int32_t)(c | (nch << 16))};
-        items.insert(items.end(), rec, rec + kItemWords);
+    std::vector<int32_t> items;
+    P.nch_token.assign(P.total_q, 0);
+    for (auto& t : tiles) {
+      const int nch = split ? (int)ceil_div(t.lim, cs) : 1;
+      if (nch > 0xFFFF) return fail(PA_ERR_UNSUPPORTED, "too many chunks per row");
+      const int64_t base = prob.causal ? (int64_t)slkv[t.b] + t.tok0 : (int64_t)slkv[t.b] + ql[t.b];
+      for (int tok = t.tok0; tok < t.tok1; ++tok) P.nch_token[cu[t.b] + tok] = nch;
+      for (int kvh = 0; kvh < prob.kv_heads; ++kvh) {
+        for (int c = 0; c < nch; ++c) {
+          const int64_t kv0 = split ? (int64_t)c * cs : 0;
+          const int64_t kv1 = split ? std::min<int64_t>(t.lim, kv0 + cs) : t.lim;
+          const int32_t rec[kItemWords] = {t.b, kvh, cu[t.b] + t.tok0, t.tok1 - t.tok0,
+                                           (int32_t)base, (int32_t)kv0, (int32_t)kv1,
+                                           (int32_t)(c | (nch << 16))};
+          items.insert(items.end(), rec, rec + kItemWords);
+        }
       }
     }
-  }
-  const int n = (int)(items.size() / kItemWords);
-  P.num_ctas = std::min(n, slots);
-  std::vector<int64_t> cost(n);
-  for (int i = 0; i < n; ++i)
-    cost[i] = ceil_div((int64_t)items[i * kItemWords + 6] - items[i * kItemWords + 5], B) + 2;
-  std::vector<int> order(n);
-  for (int i = 0; i < n; ++i) order[i] = i;
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
-  using Load = std::pair<int64_t, int>;
-  std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
-  for (int k = 0; k < P.num_ctas; ++k) heap.push({0, k});
-  std::vector<std::vector<int>> per(P.num_ctas);
-  for (int i : order) {
-    Load l = heap.top();
-    heap.pop();
-    per[l.second].push_back(i);
-    heap.push({l.first + cost[i], l.second});
-  }
-  P.work_indptr.assign(P.num_ctas + 1, 0);
-  P.items.clear();
-  P.items.reserve(items.size());
-  for (int k = 0; k < P.num_ctas; ++k) {
-    for (int i : per[k])
-      P.items.insert(P.items.end(), items.begin() + (size_t)i * kItemWords,
-                     items.begin() + (size_t)(i + 1) * kItemWords);
-    P.work_indptr[k + 1] = (int32_t)(P.items.size() / kItemWords);
+    const int n = (int)(items.size() / kItemWords);
+    P.num_ctas = std::min(n, slots);
+    std::vector<int64_t> cost(n);
+    for (int i = 0; i < n; ++i)
+      cost[i] = ceil_div((int64_t)items[i * kItemWords + 6] - items[i * kItemWords + 5], B) + 2;
+    std::vector<int> order(n);
+    for (int i = 0; i < n; ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost[a] > cost[b]; });
+    using Load = std::pair<int64_t, int>;
+    std::priority_queue<Load, std::vector<Load>, std::greater<Load>> heap;
+    for (int k = 0; k < P.num_ctas; ++k) heap.push({0, k});
+    std::vector<std::vector<int>> per(P.num_ctas);
+    for (int i : order) {
+      Load l = heap.top();
+      heap.pop();
+      per[l.second].push_back(i);
+      heap.push({l.first + cost[i], l.second});
+    }
+    P.work_indptr.assign(P.num_ctas + 1, 0);
+    P.items.clear();
+    P.items.reserve(items.size());
+    for (int k = 0; k < P.num_ctas; ++k) {
+      for (int i : per[k])
+        P.items.insert(P.items.end(), items.begin() + (size_t)i * kItemWords,
+                       items.begin() + (size_t)(i + 1) * kItemWords);
+      P.work_indptr[k + 1] = (int32_t)(P.items.size() / kItemWords);
+    }
   }
   P.max_chunks = 1;
   for (int t = 0; t < P.total_q; ++t) P.max_chunks = std::max(P.max_chunks, P.nch_token[t]);

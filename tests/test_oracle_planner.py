@@ -96,22 +96,49 @@ def test_family_selection():
 
 
 def test_auto_chunk_rule():
-    """chunk_size -1: cs = max(4B, roundup(ceil(W / (4*slots)), B)), no split when
-    that reaches the longest limit."""
+    """chunk_size -1 (GQA): cs = max(4B, roundup(ceil(W / (4*slots)), B)) with W =
+    kv_heads * sum of tile limits, no split when that reaches the longest limit."""
+    c = synth.make_case(seq_lens=[1, 2], seq_lens_kv=[4000, 9000], q_heads=8, kv_heads=2,
+                        chunk_size=-1)
+    # one tile per sequence (16 tokens per tile at G = 4): limits 4001 and 9002
+    W = 2 * (4001 + 9002)
+    assert op.plan(c, 152)["chunk"] == max(256, math.ceil(math.ceil(W / 608) / 64) * 64) == 256
+    assert op.plan(c, 2)["chunk"] == 3264       # ceil(26006 / 8) = 3251 -> 3264 < 9002
+    assert op.plan(c, 1)["chunk"] == 6528       # ceil(26006 / 4) = 6502 -> 6528 < 9002
+    big = synth.make_case(seq_lens=[1], seq_lens_kv=[100], q_heads=4, kv_heads=1,
+                          chunk_size=-1)
+    assert op.plan(big, 152)["chunk"] == 0      # 256 >= 101: no split
+
+
+def test_mla_share_rule():
+    """MLA, chunk_size -1: contiguous shares of all tiles' pages, worked by hand.
+    Tiles (one token each): limits 4001, 9001, 9002 -> 63, 141, 141 pages,
+    pages 0-62, 63-203, 204-344 (total 345).  152 SMs = 76 pairs: quota =
+    max(4, ceil(345 / 76)) = 5, 69 pairs, pair k owns pages [5k, 5k + 5)."""
     c = synth.make_case(seq_lens=[1, 2], seq_lens_kv=[4000, 9000], q_heads=128, kv_heads=1,
                         head_dim_qk=576, head_dim_v=512, kv_dtype="fp8_e4m3",
                         scale_kind="global", layout="mla", chunk_size=-1)
     P = op.plan(c, 152)
-    W = 4001 + 9001 + 9002          # lim per (token) tile
-    cs = max(256, math.ceil(math.ceil(W / (4 * 76)) / 64) * 64)
-    assert P["chunk"] == cs == 256
-    P2 = op.plan(c, 2)              # one slot: cs = roundup(22004/4) = 5504 < 9002
-    assert P2["chunk"] == 5504
-    P3 = op.plan(c, 1)              # no MLA slot pair at all -> 1 slot as well
-    assert P3["chunk"] == 5504
-    big = synth.make_case(seq_lens=[1], seq_lens_kv=[100], q_heads=4, kv_heads=1,
-                          chunk_size=-1)
-    assert op.plan(big, 152)["chunk"] == 0      # 256 >= 101: no split
+    assert P["num_ctas"] == 69 and P["chunk"] == 320
+    # pairs 0-12 touch token 0, 12-40 token 1, 40-68 token 2
+    assert P["nch_token"].tolist() == [13, 29, 29] and P["max_chunks"] == 29
+    ind, items = P["work_indptr"], P["items"]
+    # pair 12: pages 60-64 = token 0's pages 60-62 and token 1's pages 0-1
+    assert items[ind[12]:ind[13]].tolist() == [
+        [0, 0, 0, 1, 4000, 3840, 4001, 12 | (13 << 16)],
+        [1, 0, 1, 1, 9000, 0, 128, 0 | (29 << 16)]]
+    # pair 68: token 2's last pages 340-344 -> local pages 136-140
+    assert items[ind[68]:ind[69]].tolist() == [[1, 0, 2, 1, 9001, 136 * 64, 9002, 28 | (29 << 16)]]
+    # every pair holds 5 pages
+    pages = np.zeros(69, int)
+    for k in range(69):
+        for r in items[ind[k]:ind[k + 1]]:
+            pages[k] += math.ceil(r[6] / 64) - r[5] // 64
+    assert (pages == 5).all()
+    # one pair: no split, the plain items
+    P1 = op.plan(c, 2)
+    assert P1["num_ctas"] == 1 and P1["chunk"] == 0 and P1["max_chunks"] == 1
+    assert P1["items"][:, 5].tolist() == [0, 0, 0] and P1["items"][:, 6].tolist() == [4001, 9001, 9002]
 
 
 def test_workload_truncation_keeps_the_same_draws():
