@@ -106,26 +106,28 @@ def _peaks(bound: str):
 
 # DRAM bytes (read + written) per launch of each attention kernel, from one
 # ncu capture of dram__bytes_read.sum + dram__bytes_write.sum on the workload.
-# A figure is reported only while the kernel's sources still hash to the
+# A figure is reported only while the kernel's sources and the planner (which
+# decides the items, hence the partial states written) still hash to the
 # version it was taken with.
 NCU_TRAFFIC = {
     # decode-2 runs the warp-per-item kernel (at most 16 packed rows)
-    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "331e64000ff7af0d", 318.199808e6 + 4.275712e6),
+    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "397acdf58a277003", 318.197504e6 + 4.298240e6),
     # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
     # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
     # states written both grow per sequence
-    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "4acba54fe57c746b",
-                      (729.476352e6 + 31.757312e6) * 7.492152264116904),
-    "append-3": (("pa_append.cu",), "bbe9ab1be6b9dd29", 72.232704e6 + 1.659136e6),
-    "mla-5": (("pa_mla.cu",), "9e96970a85eb12ad", 199.480832e6 + 23.150848e6),
+    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "833ac25c8357e559",
+                      (729.478144e6 + 31.902208e6) * 7.492152264116904),
+    "append-3": (("pa_append.cu",), "6cab2d78e06ffcb7", 72.222208e6 + 1.779456e6),
+    "mla-5": (("pa_mla.cu",), "b504648b5c8192ef", 224.132864e6 + 7.681280e6),
 }
 
 
 def _kernel_sha(files) -> str:
-    """Hash of a kernel's source files and the headers every kernel includes."""
+    """Hash of a kernel's source files, the headers every kernel includes and
+    the planner."""
     import hashlib
     h = hashlib.sha256()
-    for n in tuple(files) + ("pa_common.cuh", "pa_ptx.cuh", "pa_internal.h"):
+    for n in tuple(files) + ("pa_common.cuh", "pa_ptx.cuh", "pa_internal.h", "pa_api.cu"):
         with open(os.path.join(ROOT, "paged_quantized_kv_gqa_gb300", "csrc", n), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
