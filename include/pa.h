@@ -320,7 +320,10 @@ pa_status pa_debug_set_faults(int64_t wait_limit_ns, int32_t skip_first_load);
  * decode kernel (tile = the warp's n-th half page): event w = warp w finished
  * it, 12 + w = warp w found it landed (passed its wait; warps 0..3).  NULL
  * disables tracing.  paged_quantized_kv_gqa_gb300/trace.py prints a summary.
- * Process-wide setting.
+ * Process-wide setting.  The stamps exist only in a library compiled with
+ * PA_TRACE (libpa_gb300_trace.so; the trace module builds and loads it): the
+ * default library has no trace code in its kernels and returns
+ * PA_ERR_UNSUPPORTED here for a non-null buffer.
  */
 pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta);
 

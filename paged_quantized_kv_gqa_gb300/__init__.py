@@ -20,7 +20,10 @@ from typing import Optional
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libpa_gb300.so")
+# PA_GB300_TRACE=1 selects the library built with the pipeline trace (the
+# trace module sets it); the default library has no trace code in its kernels
+LIB_PATH = os.path.join(_HERE, "libpa_gb300_trace.so" if os.environ.get("PA_GB300_TRACE") == "1"
+                        else "libpa_gb300.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
 PA_ERR_DEVICE_TIMEOUT, PA_ERR_BAD_PAGE = 4, 5
@@ -264,7 +267,8 @@ def pa_cache_append(plan: Plan, args: PaArgs, k_new, v_new, kv_stride: int, work
 
 def pa_debug_set_trace(buf=None, ctas: int = 0, tiles_per_cta: int = 0):
     """Enable (device uint64 buffer of ctas * tiles_per_cta * 16) or disable (None)
-    the kernels' %globaltimer pipeline trace."""
+    the kernels' %globaltimer pipeline trace (traced library only: see
+    PA_GB300_TRACE; the default library raises PA_ERR_UNSUPPORTED)."""
     _check(lib.pa_debug_set_trace(_ptr(buf), int(ctas), int(tiles_per_cta)))
 
 

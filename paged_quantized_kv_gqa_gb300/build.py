@@ -1,5 +1,9 @@
 """Builds the CUDA library (libpa_gb300.so) in-tree with nvcc for sm_103a.
 
+build(trace=True) builds the diagnostic variant libpa_gb300_trace.so instead:
+the same sources compiled with PA_TRACE, whose kernels record the pipeline
+timeline of pa_debug_set_trace (the default library carries no trace code).
+
 Translation units compile in parallel, then link into one shared library next
 to this file.  The seeded input generators (synth/csrc) are built the same way:
 the device int8 generator into synth/libpa_synth.so (nvcc) and the threaded
@@ -18,6 +22,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpa_gb300.so")
+TRACE_LIB = os.path.join(PKG, "libpa_gb300_trace.so")
 SYNTH_SRC = os.path.join(ROOT, "synth", "csrc", "synth_gen.cu")
 SYNTH_LIB = os.path.join(ROOT, "synth", "libpa_synth.so")
 SYNTH_HOST_SRC = os.path.join(ROOT, "synth", "csrc", "synth_host.c")
@@ -58,23 +63,27 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, trace: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
     deps = srcs + _headers()
-    if force or _stale(LIB, deps):
-        objs = [os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o") for s in srcs]
-        cmds = [[nvcc, *ARCH, *FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", s, "-o", o]
+    lib = TRACE_LIB if trace else LIB
+    if force or _stale(lib, deps):
+        sub = os.path.join(BUILD_DIR, "trace") if trace else BUILD_DIR
+        os.makedirs(sub, exist_ok=True)
+        defs = ["-DPA_TRACE"] if trace else []
+        objs = [os.path.join(sub, os.path.basename(s)[:-3] + ".o") for s in srcs]
+        cmds = [[nvcc, *ARCH, *FLAGS, *defs, "-I", INCLUDE, "-I", CSRC, "-c", s, "-o", o]
                 for s, o in zip(srcs, objs)]
         with cf.ThreadPoolExecutor(max_workers=max(1, min(len(cmds), os.cpu_count() or 4))) as ex:
             logs = list(ex.map(_run, cmds))
         if verbose:
             for lg in logs:
                 print(lg)
-        tmp = LIB + ".tmp"
+        tmp = lib + ".tmp"
         _run([nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
     if force or _stale(SYNTH_LIB, [SYNTH_SRC]):
         tmp = SYNTH_LIB + ".tmp"
         _run([nvcc, *ARCH, *FLAGS, "-shared", "-cudart", "shared", SYNTH_SRC, "-o", tmp])
@@ -84,7 +93,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
         _run([shutil.which("gcc") or "gcc", "-O2", "-fPIC", "-shared", "-pthread", SYNTH_HOST_SRC,
               "-o", tmp, "-lm"])
         os.replace(tmp, SYNTH_HOST_LIB)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

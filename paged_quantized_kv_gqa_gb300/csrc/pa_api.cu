@@ -681,6 +681,12 @@ pa_status pa_set_fused_merge(int32_t on) {
 }
 
 pa_status pa_debug_set_trace(void* device_buf, int32_t ctas, int32_t tiles_per_cta) {
+#ifndef PA_TRACE
+  if (device_buf)
+    return fail(PA_ERR_UNSUPPORTED,
+                "this library is built without the pipeline trace; use the traced build "
+                "(libpa_gb300_trace.so, built with PA_TRACE)");
+#endif
   if (device_buf && (ctas <= 0 || tiles_per_cta <= 0))
     return fail(PA_ERR_INVALID_ARG, "trace buffer needs positive ctas and tiles_per_cta");
   std::lock_guard<std::mutex> lk(g_fault_mu);

@@ -3,8 +3,10 @@
     python -m paged_quantized_kv_gqa_gb300.trace --config 2
     python -m paged_quantized_kv_gqa_gb300.trace --config 4
 
-Runs the workload's attention kernel a few times, then once with the
-%globaltimer trace of pa_debug_set_trace enabled, and prints a summary:
+Builds (if needed) and loads the traced library (libpa_gb300_trace.so: the
+kernels compiled with PA_TRACE), runs the workload's attention kernel a few
+times, then once with the %globaltimer trace of pa_debug_set_trace enabled,
+and prints a summary:
 
   * decode tiles of at most 16 packed rows (warp-per-item kernel): the KV bytes
     the kernel consumed per 2 us of the launch (a bandwidth-over-time profile)
@@ -95,6 +97,18 @@ def main():
     ap.add_argument("--bsz", type=int, default=0, help="keep only the first BSZ sequences")
     ap.add_argument("--save", default="", help="also write the raw stamps to this .npz file")
     args = ap.parse_args()
+
+    if os.environ.get("PA_GB300_TRACE") != "1":
+        # the package loads its library on import: build the traced one and
+        # start again with it selected
+        import importlib.util
+        spec = importlib.util.spec_from_file_location(
+            "pa_build", os.path.join(ROOT, "paged_quantized_kv_gqa_gb300", "build.py"))
+        bmod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(bmod)
+        bmod.build(trace=True)
+        os.environ["PA_GB300_TRACE"] = "1"
+        os.execv(sys.executable, [sys.executable, "-m", "paged_quantized_kv_gqa_gb300.trace", *sys.argv[1:]])
 
     import torch
     import synth

@@ -161,3 +161,13 @@ def test_run_rejects_null_pointers_before_launch(pa):
     with pytest.raises(pa.PaError) as e:
         pa.pa_run(plan, args2, 256, None)
     assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
+def test_default_library_has_no_pipeline_trace(pa):
+    """The pipeline trace exists only in the library built with PA_TRACE: the
+    default one refuses a trace buffer (host-side check, no GPU needed) and
+    accepts turning the trace off."""
+    import ctypes
+    assert pa.lib.pa_debug_set_trace(ctypes.c_void_p(256), 1, 1) == pa.PA_ERR_UNSUPPORTED
+    assert "PA_TRACE" in pa.pa_last_error()
+    assert pa.lib.pa_debug_set_trace(None, 0, 0) == pa.PA_OK
