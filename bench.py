@@ -111,14 +111,14 @@ def _peaks(bound: str):
 # version it was taken with.
 NCU_TRAFFIC = {
     # decode-2 runs the warp-per-item kernel (at most 16 packed rows)
-    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "397acdf58a277003", 318.197504e6 + 4.298240e6),
+    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "8073854d6a09f30c", 318.206464e6 + 4.213504e6),
     # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
     # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
     # states written both grow per sequence
-    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "833ac25c8357e559",
-                      (729.478144e6 + 31.902208e6) * 7.492152264116904),
-    "append-3": (("pa_append.cu",), "6cab2d78e06ffcb7", 72.222208e6 + 1.779456e6),
-    "mla-5": (("pa_mla.cu",), "b504648b5c8192ef", 224.132864e6 + 7.681280e6),
+    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "498b21babf77403a",
+                      (729.512192e6 + 31.749888e6) * 7.492152264116904),
+    "append-3": (("pa_append.cu",), "92ca7c1e1b888c76", 72.250368e6 + 1.828864e6),
+    "mla-5": (("pa_mla.cu",), "e43e804031f84123", 224.423680e6 + 7.286528e6),
 }
 
 
