@@ -805,28 +805,47 @@ __global__ void __launch_bounds__(kThreads, 1)
       fail = true;
     };
     // Q' of an item -> shared memory buffer qb (fp16, K-major, 128B swizzle, padded rows zero)
+    // A thread's pieces are rows d/16 + 8k, dims 8 (d & 15) .. +7: every
+    // load is issued before the first conversion, so their latencies overlap
+    // (a shared-memory store between two loads would order them).
     auto load_q = [&](const Item& m, uint32_t qb) {
+      constexpr int kPieces = NR * 16 / 128;
+      static_assert(NR * 16 % 128 == 0, "whole 16-byte pieces per thread");
       const int n_rows = m.ntok * G;
-      for (int task = d; task < NR * 16; task += 128) {
-        const int r = task >> 4, ch = task & 15;
-        uint4 packed = make_uint4(0, 0, 0, 0);
+      const int ch = d & 15;
+      uint4 raw[kPieces];
+#pragma unroll
+      for (int k = 0; k < kPieces; ++k) {
+        const int r = (d >> 4) + 8 * k;
+        raw[k] = make_uint4(0, 0, 0, 0);
         if (r < n_rows) {
           const int token = m.tok0 + r / G;
           const int head = m.kvh * G + r % G;
-          const uint4 raw = *reinterpret_cast<const uint4*>(p.q + (int64_t)token * p.q_stride +
-                                                            head * kHeadDim + ch * 8);
-          const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw);
+          raw[k] = *reinterpret_cast<const uint4*>(p.q + (int64_t)token * p.q_stride +
+                                                   head * kHeadDim + ch * 8);
+        }
+      }
+      // per-channel K scales of these 8 dims (1 otherwise: x * 1 is exact)
+      float sc[8];
+      if (p.scale_kind == PA_SCALE_PER_CHANNEL) {
+        const uint4 sr = *reinterpret_cast<const uint4*>(
+            reinterpret_cast<const __nv_bfloat16*>(p.k_scale) + m.kvh * kHeadDim + ch * 8);
+        const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(&sr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc[e] = __bfloat162float(sv[e]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc[e] = 1.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < kPieces; ++k) {
+        const int r = (d >> 4) + 8 * k;
+        uint4 packed = make_uint4(0, 0, 0, 0);
+        if (r < n_rows) {
+          const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&raw[k]);
           float f[8];
-          if (p.scale_kind == PA_SCALE_PER_CHANNEL) {
-            const uint4 sr = *reinterpret_cast<const uint4*>(
-                reinterpret_cast<const __nv_bfloat16*>(p.k_scale) + m.kvh * kHeadDim + ch * 8);
-            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(&sr);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]) * __bfloat162float(sv[e]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]);
-          }
+          for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]) * sc[e];
           packed.x = pack_half2(f[0], f[1]);
           packed.y = pack_half2(f[2], f[3]);
           packed.z = pack_half2(f[4], f[5]);
