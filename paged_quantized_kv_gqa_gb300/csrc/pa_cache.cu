@@ -10,12 +10,15 @@
 // its scale, then int8 round-half-even saturated to +-127, or E4M3
 // round-to-nearest-even saturated to +-448.
 //
-// One CTA per (sequence, page of the appended range, kv head).  When the new
-// rows are 16-byte aligned (GQA), each thread reads 8 dims of a position per
-// 16-byte load (all of a page's loads in flight at once), writes 8-byte K row
-// pieces, and V goes through shared memory so that thread = dim writes its V^T
-// row 16 bytes at a time.  Otherwise (and for MLA rows) thread = dim with
-// 2-byte reads, 16 positions' loads in flight before their stores.
+// When the new rows are 16-byte aligned (GQA), one CTA per (sequence,
+// 16-position chunk of the appended range aligned to the page's 16-position
+// boundaries, kv head): each thread reads 8 dims of two positions with 16-byte
+// loads, writes 8-byte K row pieces, and V goes through shared memory so that
+// thread = dim writes its V^T row piece of the chunk as one 16-byte store (the
+// small chunks give the GPU enough warps to hide the loads' latency and the
+// correctly rounded divisions).  Otherwise (and for MLA rows) one CTA per
+// (sequence, page of the appended range, kv head), thread = dim with 2-byte
+// reads, 16 positions' loads in flight before their stores.
 #include "pa_common.cuh"
 
 namespace pa {
@@ -23,6 +26,7 @@ namespace {
 
 constexpr int kPage = 64;
 constexpr int kThreads = 128;
+constexpr int kChunk = 16;       // positions per CTA on the 16-byte path
 
 template <int FP8>
 __device__ __forceinline__ uint8_t quantize(float x, float s) {
@@ -66,19 +70,29 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
   if (q <= 0) return;
   const int start = p.seq_lens_kv[b];
   const int end = start + q;
-  const int lp = start / kPage + (int)blockIdx.y;
-  const int p0 = max(lp * kPage, start), p1 = min(lp * kPage + kPage, end);
+  // this CTA's positions [p0, p1) and their page: a 16-position chunk on the
+  // 16-byte path, else a page
+  const int unit = VEC ? kChunk : kPage;
+  const int u0 = (start / unit + (int)blockIdx.y) * unit;
+  const int p0 = max(u0, start), p1 = min(u0 + unit, end);
   if (p0 >= p1) return;
-  const int page = p.block_table[(int64_t)b * p.max_blocks + lp];
-  if (page < 0 || page >= p.num_pages) {
+  const int lp = u0 / kPage;
+  // the positions' page id; false (and the status recorded) when it is not a
+  // page of the cache.  Read after the new rows' loads are issued where the
+  // path allows, so that the two round trips overlap.
+  auto page_of = [&](int& page) -> bool {
+    page = p.block_table[(int64_t)b * p.max_blocks + lp];
+    if (page >= 0 && page < p.num_pages) return true;
     if (threadIdx.x == 0 && atomicCAS(p.status, 0, PA_ERR_BAD_PAGE) == 0) {
       p.status[1] = b;
       p.status[2] = (int)blockIdx.x;
     }
-    return;
-  }
+    return false;
+  };
   const int t0 = p.cu_seqlens_q[b] + (p0 - start);
   if (p.mla) {
+    int page;
+    if (!page_of(page)) return;
     // whole latent rows: row pos -> cache[page][pos % 64][0 .. 576); eight
     // positions' loads are in flight before any store
     const float s = reinterpret_cast<const float*>(p.k_scale)[0];
@@ -107,15 +121,12 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
     }
     return;
   }
-  const int64_t slab = (int64_t)page * p.kv_heads + kvh;
   if constexpr (VEC) {
-    // 16-byte rows in and out: thread t reads dims 8 (t & 15) .. + 7 of
-    // positions (t >> 4) + 8 k, writes those 8 K bytes into the K row, and
-    // stages the 8 V bytes in shared memory [position][dim]; then thread = dim
-    // gathers its V^T row segment and writes it 16 bytes at a time
-    __shared__ __align__(16) uint8_t vs[kPage][128];
+    // thread t: dims 8 (t & 15) .. + 7 of chunk positions u0 + (t >> 4) and
+    // u0 + (t >> 4) + 8; the V bytes are staged [position][dim], then thread =
+    // dim writes its V^T row piece of the chunk
+    __shared__ __align__(16) uint8_t vs[kChunk][128];
     const int c8 = threadIdx.x & 15, r8 = threadIdx.x >> 4;
-    const int n = p1 - p0;
     float sk[8], sv[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
@@ -123,22 +134,24 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
       sk[e] = load_scale(p.k_scale, p.scale_kind, idx);
       sv[e] = load_scale(p.v_scale, p.scale_kind, idx);
     }
-    uint8_t* kpage = p.cache_k + slab * kPage * 128;
-    uint4 rk[8], rv[8];
+    uint4 rk[2], rv[2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int pos = r8 + 8 * k;
-      if (pos < n) {
-        const int64_t src = (int64_t)(t0 + pos) * p.kv_stride + (int64_t)kvh * 128 + 8 * c8;
+    for (int k = 0; k < 2; ++k) {
+      const int pos = u0 + r8 + 8 * k;
+      if (pos >= p0 && pos < p1) {
+        const int64_t src = (int64_t)(t0 + pos - p0) * p.kv_stride + (int64_t)kvh * 128 + 8 * c8;
         rk[k] = *reinterpret_cast<const uint4*>(p.k_new + src);
         rv[k] = *reinterpret_cast<const uint4*>(p.v_new + src);
       }
     }
+    int page;
+    if (!page_of(page)) return;   // uniform over the CTA: no thread reaches the barrier below
+    const int64_t slab = (int64_t)page * p.kv_heads + kvh;
+    uint8_t* kpage = p.cache_k + slab * kPage * 128;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int pos = r8 + 8 * k;
-      if (pos < n) {
-        const int off = (p0 + pos) % kPage;
+    for (int k = 0; k < 2; ++k) {
+      const int pos = u0 + r8 + 8 * k;
+      if (pos >= p0 && pos < p1) {
         const __nv_bfloat16* hk = reinterpret_cast<const __nv_bfloat16*>(&rk[k]);
         const __nv_bfloat16* hv = reinterpret_cast<const __nv_bfloat16*>(&rv[k]);
         uint32_t wk[2] = {0, 0}, wv[2] = {0, 0};
@@ -147,28 +160,27 @@ __global__ void __launch_bounds__(kThreads) cache_append_kernel(const AppendPara
           wk[e >> 2] |= (uint32_t)quantize<FP8>(__bfloat162float(hk[e]), sk[e]) << (8 * (e & 3));
           wv[e >> 2] |= (uint32_t)quantize<FP8>(__bfloat162float(hv[e]), sv[e]) << (8 * (e & 3));
         }
-        *reinterpret_cast<uint2*>(kpage + off * 128 + 8 * c8) = make_uint2(wk[0], wk[1]);
-        *reinterpret_cast<uint2*>(&vs[off][8 * c8]) = make_uint2(wv[0], wv[1]);
+        *reinterpret_cast<uint2*>(kpage + (pos % kPage) * 128 + 8 * c8) = make_uint2(wk[0], wk[1]);
+        *reinterpret_cast<uint2*>(&vs[pos - u0][8 * c8]) = make_uint2(wv[0], wv[1]);
       }
     }
     __syncthreads();
     const int d = threadIdx.x;
     uint8_t* vrow = p.cache_v + (slab * 128 + d) * kPage;
-    const int a = p0 % kPage, e_end = a + n;
-    for (int base = a; base < e_end;) {
-      const int next = min(e_end, (base / 16 + 1) * 16);
-      if (next - base == 16) {
-        uint32_t w[4] = {0, 0, 0, 0};
+    if (p0 == u0 && p1 == u0 + kChunk) {
+      uint32_t w[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) w[j >> 2] |= (uint32_t)vs[base + j][d] << (8 * (j & 3));
-        *reinterpret_cast<uint4*>(vrow + base) = make_uint4(w[0], w[1], w[2], w[3]);
-      } else {
-        for (int j = base; j < next; ++j) vrow[j] = vs[j][d];
-      }
-      base = next;
+      for (int j = 0; j < kChunk; ++j) w[j >> 2] |= (uint32_t)vs[j][d] << (8 * (j & 3));
+      *reinterpret_cast<uint4*>(vrow + u0 % kPage) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+      // a ragged end of the appended range: only its own positions' bytes
+      for (int pos = p0; pos < p1; ++pos) vrow[pos % kPage] = vs[pos - u0][d];
     }
     return;
   }
+  int page;
+  if (!page_of(page)) return;
+  const int64_t slab = (int64_t)page * p.kv_heads + kvh;
   const int d = threadIdx.x;   // head dim (GQA head_dim 128)
   const float sk = load_scale(p.k_scale, p.scale_kind,
                               p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh * 128 + d : kvh);
@@ -235,12 +247,14 @@ cudaError_t launch_cache_append(const Plan& plan, const pa_args& a, const void* 
   p.head_dim = pr.head_dim_qk;
   p.scale_kind = pr.scale_kind;
   p.mla = pr.layout == PA_LAYOUT_MLA ? 1 : 0;
-  // pages an appended range of max_q positions can touch
-  const int npg = (plan.max_q + kPage - 1) / kPage + 1;
-  const dim3 grid(pr.bsz, npg, p.mla ? 1 : pr.kv_heads);
   // 16-byte row access when the new rows allow it (GQA only)
   const bool vec = !p.mla && kv_stride % 8 == 0 && reinterpret_cast<uintptr_t>(k_new) % 16 == 0 &&
                    reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
+  // 16-position chunks (16-byte path) or pages an appended range of max_q
+  // positions can touch
+  const int unit = vec ? kChunk : kPage;
+  const int nunits = (plan.max_q + unit - 1) / unit + 1;
+  const dim3 grid(pr.bsz, nunits, p.mla ? 1 : pr.kv_heads);
   if (pr.kv_dtype == PA_KV_FP8_E4M3) {
     if (vec) cache_append_kernel<1, true><<<grid, kThreads, 0, stream>>>(p);
     else cache_append_kernel<1, false><<<grid, kThreads, 0, stream>>>(p);
