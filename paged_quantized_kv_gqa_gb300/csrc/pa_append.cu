@@ -500,6 +500,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool pc = p.scale_kind == PA_SCALE_PER_CHANNEL;
       const __nv_bfloat16* ksc =
           reinterpret_cast<const __nv_bfloat16*>(p.k_scale) + m.kvh * kHeadDim;
+      // a thread's pieces all hold dims 8 (t & 15) .. + 7: their per-channel K
+      // scales are read once, before the loop (inside it, each read would
+      // wait for the previous piece's shared-memory store)
+      float sc[8];
+      if (pc) {
+        const uint4 sr = *reinterpret_cast<const uint4*>(ksc + (t & 15) * 8);
+        const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(&sr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sc[e] = __bfloat162float(sv[e]);
+      }
       if (!wait_or_abort(qfull, li & 1, limit, abort_any)) { note_fail(it); break; }
       // Q' = bf16 Q (times the per-channel K scale) -> fp16, in place
       for (int task = t; task < kRows * 16; task += 128) {
@@ -512,10 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 8; ++e) f[e] = __bfloat162float(hv[e]);
         if (pc) {
-          const uint4 sr = *reinterpret_cast<const uint4*>(ksc + ch * 8);
-          const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(&sr);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) f[e] *= __bfloat162float(sv[e]);
+          for (int e = 0; e < 8; ++e) f[e] *= sc[e];
         }
         uint4 packed;
         packed.x = pack_half2(f[0], f[1]);
