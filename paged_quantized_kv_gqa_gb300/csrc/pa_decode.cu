@@ -413,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             slot0[r] = (int64_t)tok[r] * p.max_chunks * p.q_heads + head[r];
           }
           float acc[kMergeRows][kHeadDim / 32], M[kMergeRows], W[kMergeRows];
-          merge_rows<kHeadDim, kMergeRows>(p.part_o, p.part_m, p.part_d, slot0, valid, p.q_heads, m.nch,
+          merge_rows<kHeadDim, kMergeRows, 4>(p.part_o, p.part_m, p.part_d, slot0, valid, p.q_heads, m.nch,
                                   lane, acc, M, W);
 #pragma unroll
           for (int r = 0; r < kMergeRows; ++r)

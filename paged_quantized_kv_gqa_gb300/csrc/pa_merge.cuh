@@ -16,12 +16,13 @@
 namespace pa {
 
 // Merges R rows with one warp (all lanes call it; rows with valid[r] false
-// come out with W = 0).  The partial states are read through L2 only (other
+// come out with W = 0); U chunk rows of each row are read per pass (the merge
+// kernel's default; a caller short of registers passes fewer).  The partial states are read through L2 only (other
 // CTAs of the same launch may have written them).  Lane l owns output elements
 // [l * DV / 32, + DV / 32); lane c holds the weight of chunk c0 + c, and each
 // row's chunk vectors are read several chunks at a time so that their loads
 // are in flight together.
-template <int DV, int R>
+template <int DV, int R, int U = (DV >= 512 ? 2 : 8)>
 __device__ __forceinline__ void merge_rows(const __nv_bfloat16* __restrict__ part_o,
                                            const float* __restrict__ part_m,
                                            const float* __restrict__ part_d,
@@ -32,10 +33,12 @@ __device__ __forceinline__ void merge_rows(const __nv_bfloat16* __restrict__ par
   static_assert(kPer % 4 == 0, "lane slice must be a multiple of 4 elements");
   // a lane reads its slice of a chunk row as 16-byte vectors where it can (8
   // bf16), else 8-byte ones; kU chunk rows are in flight per pass (fewer for
-  // wide rows, to keep the registers and hence the occupancy up)
+  // wide rows, to keep the registers and hence the occupancy up).  Measured in
+  // the merge kernel on rows of 8-33 chunks (128 wide) and 2-4 chunks (512
+  // wide): 4 -> 8 rows 99 -> 93 us, 16 rows 119 us; 1 -> 2 wide rows 15 -> 13 us.
   constexpr int kVecBytes = (kPer % 8 == 0) ? 16 : 8;
   constexpr int kVec = kPer * 2 / kVecBytes;
-  constexpr int kU = DV >= 512 ? 1 : 4;
+  constexpr int kU = U;
   float m0[R], d0[R];   // chunk `lane` of each row (the first pass of 32)
 #pragma unroll
   for (int r = 0; r < R; ++r) {
