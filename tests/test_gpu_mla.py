@@ -41,6 +41,29 @@ def test_mla_edge_cases(kw):
     compare(case, out, lse, label=str(kw))
 
 
+# the planner's contiguous page shares on a small grid: several short tokens
+# share a pair, and shares cut tokens at page boundaries (8 SMs = 4 pairs;
+# 11 pages -> shares of 4 pages), causal and not
+SHARES = [
+    dict(seq_lens=[1, 1, 1, 2, 1], seq_lens_kv=[10, 70, 0, 130, 5], chunk_size=-1),
+    dict(seq_lens=[2, 1], seq_lens_kv=[300, 190], chunk_size=-1, causal=False),
+]
+
+
+@pytest.mark.parametrize("kw", SHARES)
+def test_mla_page_shares(kw):
+    case = _mla_case(23, **kw)
+    out, lse, plan, _, _ = run_case(case, sms=8)
+    d = plan.describe()
+    assert d["family"] == "mla" and d["max_chunks"] > 1
+    # every pair holds at most `quota` pages and the pieces of a token are in position order
+    items, ind = d["items"], d["work_indptr"]
+    for k in range(d["num_ctas"]):
+        pages = sum(-(-int(r[6]) // 64) - int(r[5]) // 64 for r in items[ind[k]:ind[k + 1]])
+        assert pages <= d["chunk"] // 64
+    compare(case, out, lse, label=str(kw))
+
+
 def test_mla_5_full():
     """Full-size MLA workload (bsz 32, q_len U{1,2}, prefix U[4096,16384], fp8
     global scale, automatic split + merge) in the benchmark's launch
