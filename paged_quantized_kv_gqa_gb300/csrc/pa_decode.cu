@@ -86,6 +86,76 @@ __device__ __forceinline__ bool dwait(uint64_t* bar, uint32_t parity, uint64_t l
   return wait_or_abort(bar, parity, limit_ns, abort_any, 32);
 }
 
+// Sums n values per thread (one per row) over the 32 lanes of a warp, all rows
+// at once.  While n is even, each exchange sends half of the rows still held to
+// the partner lane and keeps the other half (the lane with the offset bit set
+// keeps the upper half), so the warp spends n/2 + n/4 + ... shuffles instead of
+// 5 n; once n is odd the remaining offsets exchange everything.  On return v[0
+// .. left) holds the sums of rows row0 .. row0 + left - 1, and the lanes that
+// differ only in the bits of the full exchanges hold the same values.
+template <int N, int O>
+__device__ __forceinline__ void sum_rows_step(float* v, int lane, int& row0) {
+  if constexpr (N % 2 == 0 && N > 1) {
+    constexpr int H = N / 2;
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+      const float send = up ? v[k] : v[k + H];
+      const float keep = up ? v[k + H] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, O);
+    }
+    if (up) row0 += H;
+    if constexpr (O > 1) sum_rows_step<H, O / 2>(v, lane, row0);
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] += __shfl_xor_sync(0xffffffffu, v[k], O);
+    if constexpr (O > 1) sum_rows_step<N, O / 2>(v, lane, row0);
+  }
+}
+
+// The same exchange for the row maxima.  The first step reads the tile's
+// values and writes half as many, so that they stay intact for the softmax.
+template <int N, int O>
+__device__ __forceinline__ void max_rows_step(float* v, int lane, int& row0) {
+  if constexpr (N % 2 == 0 && N > 1) {
+    constexpr int H = N / 2;
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+      const float send = up ? v[k] : v[k + H];
+      const float keep = up ? v[k + H] : v[k];
+      v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+    }
+    if (up) row0 += H;
+    if constexpr (O > 1) max_rows_step<H, O / 2>(v, lane, row0);
+  } else {
+#pragma unroll
+    for (int k = 0; k < N; ++k) v[k] = fmaxf(v[k], __shfl_xor_sync(0xffffffffu, v[k], O));
+    if constexpr (O > 1) max_rows_step<N, O / 2>(v, lane, row0);
+  }
+}
+template <int N>
+__device__ __forceinline__ void max_rows_first(const float* s, float* t, int lane, int& row0) {
+  constexpr int H = N / 2;
+  const bool up = (lane & 16) != 0;
+#pragma unroll
+  for (int k = 0; k < H; ++k) {
+    const float send = up ? s[k] : s[k + H];
+    const float keep = up ? s[k + H] : s[k];
+    t[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+  }
+  if (up) row0 += H;
+  max_rows_step<H, 8>(t, lane, row0);
+}
+
+// rows one lane holds after sum_rows_step<N, 16>
+template <int N, int O = 16>
+constexpr int sum_rows_left() {
+  if constexpr (O == 0) return N;
+  else if constexpr (N % 2 == 0 && N > 1) return sum_rows_left<N / 2, O / 2>();
+  else return sum_rows_left<N, O / 2>();
+}
+
 // Page-stage ring depth.  Three stages measured faster than four at every
 // row count (48 rows: 1.56-1.65 -> 1.527 ms on spec-verify-4; 32 rows 0.611
 // -> 0.601 ms): the copies still run well ahead of the converter.
@@ -665,11 +735,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // exact tile maximum per row, new running max; rescale l (registers)
-          // and this half's columns of O (TMEM) by 2^(m_old - m_new)
+          // and this half's columns of O (TMEM) by 2^(m_old - m_new).  Up to
+          // 24 rows per warpgroup the warp maxima come from the halving
+          // exchange (48 rows: 5 % faster than one redux.sync per row)
+          if constexpr (NH <= 24) {
+            constexpr int kLeft = sum_rows_left<NH>();
+            constexpr int kDup = 32 * kLeft / NH;
+            float t[NH / 2];
+            int row0 = 0;
+            max_rows_first<NH>(s, t, lane, row0);
+            if ((lane & (kDup - 1)) == 0) {
 #pragma unroll
-          for (int j = 0; j < NH; ++j) {
-            const float wm = warp_max(s[j]);
-            if (lane == 0) red[(warp & 3) * NR + r_lo + j] = wm;
+              for (int k = 0; k < kLeft; ++k) red[(warp & 3) * NR + r_lo + row0 + k] = t[k];
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < NH; ++j) {
+              const float wm = warp_max(s[j]);
+              if (lane == 0) red[(warp & 3) * NR + r_lo + j] = wm;
+            }
           }
           bar_sync(bar_id, 128);
           if (pos_in_tile < NH) {
@@ -685,9 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             alpha_s[r] = a;
           }
           bar_sync(bar_id, 128);
-#pragma unroll
-          for (int j = 0; j < NH; ++j) l[j] *= alpha_s[r_lo + j];
           if (i > 0) {
+#pragma unroll
+            for (int j = 0; j < NH; ++j) l[j] *= alpha_s[r_lo + j];
             // O holds PV of the earlier tiles of this item: wait for the last one
             if (!fail && !dwait(&pvdone[(g - 1) & 3], ((g - 1) >> 2) & 1, limit, abort_any))
               note_fail(it);
@@ -756,13 +840,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (i + 1 == cur.ntiles) {
           // row sums over all positions of the item: warp, then warpgroup; the
-          // owner thread of row r keeps 1/l and writes the row statistics
+          // owner thread of row r keeps 1/l and writes the row statistics.
+          // Up to 24 rows per warpgroup the halving exchange is used (48 rows:
+          // 27 shuffles a thread instead of 120); at 32 rows it measured
+          // slower than one butterfly per row (more spilled registers)
+          if constexpr (NH <= 24) {
+            constexpr int kLeft = sum_rows_left<NH>();
+            constexpr int kDup = 32 * kLeft / NH;   // lanes holding the same rows
+            int row0 = 0;
+            sum_rows_step<NH, 16>(l, lane, row0);
+            if ((lane & (kDup - 1)) == 0) {
 #pragma unroll
-          for (int j = 0; j < NH; ++j) {
-            float v = l[j];
+              for (int k = 0; k < kLeft; ++k) red_l[(warp & 3) * NR + r_lo + row0 + k] = l[k];
+            }
+          } else {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) red_l[(warp & 3) * NR + r_lo + j] = v;
+            for (int j = 0; j < NH; ++j) {
+              float v = l[j];
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+              if (lane == 0) red_l[(warp & 3) * NR + r_lo + j] = v;
+            }
           }
           bar_sync(bar_id, 128);
           if (pos_in_tile < NH) {
