@@ -115,8 +115,8 @@ NCU_TRAFFIC = {
     # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
     # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
     # states written both grow per sequence
-    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "25088fba4ebf7f94",
-                      (729.601536e6 + 32.264960e6) * 7.492152264116904),
+    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "38c2b23f35bc3662",
+                      (729.481984e6 + 31.984896e6) * 7.492152264116904),
     "append-3": (("pa_append.cu",), "92ca7c1e1b888c76", 72.250368e6 + 1.828864e6),
     "mla-5": (("pa_mla.cu",), "e43e804031f84123", 224.423680e6 + 7.286528e6),
 }
