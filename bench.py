@@ -111,14 +111,14 @@ def _peaks(bound: str):
 # version it was taken with.
 NCU_TRAFFIC = {
     # decode-2 runs the warp-per-item kernel (at most 16 packed rows)
-    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "8073854d6a09f30c", 318.206464e6 + 4.213504e6),
+    "decode-2": (("pa_decode_warp.cu", "pa_index.cuh"), "43caaa15a0fbd4dc", 318.204928e6 + 4.337920e6),
     # captured on the first 16 of the 128 sequences (726.5 MB of the 5443 MB
     # cache) and scaled by the KV-bytes ratio 7.4922: pages read and partial
     # states written both grow per sequence
-    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "38c2b23f35bc3662",
-                      (729.481984e6 + 31.984896e6) * 7.492152264116904),
-    "append-3": (("pa_append.cu",), "92ca7c1e1b888c76", 72.250368e6 + 1.828864e6),
-    "mla-5": (("pa_mla.cu",), "e43e804031f84123", 224.423680e6 + 7.286528e6),
+    "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "3545fe789aae18a8",
+                      (729.481728e6 + 31.898112e6) * 7.492152264116904),
+    "append-3": (("pa_append.cu",), "1d5e961f8bec2af9", 72.213760e6 + 1.729536e6),
+    "mla-5": (("pa_mla.cu",), "bdf0753cd25ebc74", 224.310784e6 + 6.930432e6),
 }
 
 

@@ -52,7 +52,9 @@ typedef enum pa_status {
   PA_ERR_UNSUPPORTED = 2,   /* valid problem outside the compiled kernel set  */
   PA_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed              */
   PA_ERR_DEVICE_TIMEOUT = 4,/* a kernel's bounded wait ran out (see pa_check) */
-  PA_ERR_BAD_PAGE = 5       /* a block-table entry outside [0, num_pages)     */
+  PA_ERR_BAD_PAGE = 5,      /* a block-table entry outside [0, num_pages)     */
+  PA_ERR_BAD_ITEM = 6       /* debug library only: a work item outside the
+                               problem's bounds (see pa_check)                */
 } pa_status;
 
 enum { PA_KV_INT8 = 0, PA_KV_FP8_E4M3 = 1 };
@@ -227,8 +229,16 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
 pa_status pa_merge(const pa_plan_t* plan, const pa_args* args, void* workspace, void* stream);
 
 /* Synchronises the stream, then reads the workspace status word.  Returns
- * PA_OK, PA_ERR_DEVICE_TIMEOUT or PA_ERR_BAD_PAGE; *detail (may be NULL) gets
- * the recorded item / CTA detail. */
+ * PA_OK, PA_ERR_DEVICE_TIMEOUT or PA_ERR_BAD_PAGE (or, from the debug library,
+ * PA_ERR_BAD_ITEM); *detail (may be NULL) gets the recorded item / CTA detail.
+ *
+ * Debug library: libpa_gb300_debug.so, the same sources compiled with
+ * PA_DEBUG (the Python binding loads it when PA_GB300_DEBUG=1).  Its attention
+ * kernels check every work item of a CTA against the problem's bounds before
+ * any work (a bad item: PA_ERR_BAD_ITEM, detail = item index, and the CTA does
+ * nothing), and fill shared memory (0xFF bytes) and their TMEM columns
+ * (0xFFFFFFFF) before first use, so that a read of memory the kernel never
+ * wrote shows as NaN in the output.  The default library has none of this. */
 pa_status pa_check(const pa_plan_t* plan, const void* workspace, void* stream, int32_t* detail);
 
 void pa_plan_destroy(pa_plan_t* plan);

@@ -21,12 +21,14 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 # PA_GB300_TRACE=1 selects the library built with the pipeline trace (the
-# trace module sets it); the default library has no trace code in its kernels
+# trace module sets it); PA_GB300_DEBUG=1 the debug library (work-item bounds
+# checks, poisoned shared and tensor memory); the default library has neither
 LIB_PATH = os.path.join(_HERE, "libpa_gb300_trace.so" if os.environ.get("PA_GB300_TRACE") == "1"
+                        else "libpa_gb300_debug.so" if os.environ.get("PA_GB300_DEBUG") == "1"
                         else "libpa_gb300.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_CUDA = 0, 1, 2, 3
-PA_ERR_DEVICE_TIMEOUT, PA_ERR_BAD_PAGE = 4, 5
+PA_ERR_DEVICE_TIMEOUT, PA_ERR_BAD_PAGE, PA_ERR_BAD_ITEM = 4, 5, 6
 KV_DTYPES = {"int8": 0, "fp8_e4m3": 1}
 SCALE_KINDS = {"per_kv_head": 0, "per_channel": 1, "global": 2}
 LAYOUTS = {"gqa": 0, "mla": 1}

@@ -3,6 +3,9 @@
 build(trace=True) builds the diagnostic variant libpa_gb300_trace.so instead:
 the same sources compiled with PA_TRACE, whose kernels record the pipeline
 timeline of pa_debug_set_trace (the default library carries no trace code).
+build(debug=True) builds libpa_gb300_debug.so: the sources compiled with
+PA_DEBUG (work-item bounds checks, shared and tensor memory poisoned before
+first use).
 
 Translation units compile in parallel, then link into one shared library next
 to this file.  The seeded input generators (synth/csrc) are built the same way:
@@ -23,6 +26,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libpa_gb300.so")
 TRACE_LIB = os.path.join(PKG, "libpa_gb300_trace.so")
+DEBUG_LIB = os.path.join(PKG, "libpa_gb300_debug.so")
 SYNTH_SRC = os.path.join(ROOT, "synth", "csrc", "synth_gen.cu")
 SYNTH_LIB = os.path.join(ROOT, "synth", "libpa_synth.so")
 SYNTH_HOST_SRC = os.path.join(ROOT, "synth", "csrc", "synth_host.c")
@@ -63,16 +67,18 @@ def _run(cmd):
     return r.stdout + r.stderr
 
 
-def build(verbose: bool = False, force: bool = False, trace: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False, trace: bool = False, debug: bool = False) -> str:
+    if trace and debug:
+        raise ValueError("the trace and debug libraries are separate builds")
     os.makedirs(BUILD_DIR, exist_ok=True)
     nvcc = _nvcc()
     srcs = _sources()
     deps = srcs + _headers()
-    lib = TRACE_LIB if trace else LIB
+    lib = TRACE_LIB if trace else DEBUG_LIB if debug else LIB
     if force or _stale(lib, deps):
-        sub = os.path.join(BUILD_DIR, "trace") if trace else BUILD_DIR
+        sub = os.path.join(BUILD_DIR, "trace") if trace else os.path.join(BUILD_DIR, "debug") if debug else BUILD_DIR
         os.makedirs(sub, exist_ok=True)
-        defs = ["-DPA_TRACE"] if trace else []
+        defs = ["-DPA_TRACE"] if trace else ["-DPA_DEBUG"] if debug else []
         objs = [os.path.join(sub, os.path.basename(s)[:-3] + ".o") for s in srcs]
         cmds = [[nvcc, *ARCH, *FLAGS, *defs, "-I", INCLUDE, "-I", CSRC, "-c", s, "-o", o]
                 for s, o in zip(srcs, objs)]

@@ -527,6 +527,9 @@ pa_status pa_run(const pa_plan_t* plan, const pa_args* args, void* workspace, vo
   p.trace = fc.trace;
   p.trace_ctas = fc.trace_ctas;
   p.trace_tiles = fc.trace_tiles;
+  p.bsz = pr.bsz;
+  p.total_q = plan->total_q;
+  p.num_items = (int32_t)(plan->items.size() / kItemWords);
   p.sm_scale_log2 = pr.sm_scale * 1.4426950408889634f;
   p.ep = epilogue_of(*args);
   p.cu_seqlens_q = args->cu_seqlens_q;

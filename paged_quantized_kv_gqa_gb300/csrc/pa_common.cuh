@@ -40,6 +40,59 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, ui
   }
 }
 
+// ---------------------------------------------------------------- debug build
+// The debug library (libpa_gb300_debug.so, compiled with PA_DEBUG) adds, in
+// every attention kernel:
+//   * a check of the CTA's work items against the problem's bounds before any
+//     work (sequence, kv head, query tokens, kv range within the block table,
+//     chunk index); a bad item is recorded as PA_ERR_BAD_ITEM with its index
+//     and the CTA leaves at once, before it allocates or initialises anything;
+//   * shared memory filled with 0xFF bytes before first use (NaN as fp16, bf16
+//     and fp32), so a read of a byte the kernel never wrote reaches the output
+//     as NaN;
+//   * the allocated TMEM columns filled with 0xFFFFFFFF (NaN) the same way.
+// In the default library the macros below expand to nothing.
+constexpr int kDebugPage = 64;   // positions per block-table entry
+
+#ifdef PA_DEBUG
+static __device__ __noinline__ bool debug_items_ok(const AttnParams& p, int begin, int end);
+
+// Every thread of the CTA calls this before the first write to shared memory.
+__device__ __forceinline__ void debug_poison_smem(uint8_t* smem, int bytes) {
+  for (int i = (int)threadIdx.x * 16; i + 16 <= bytes; i += (int)blockDim.x * 16)
+    *reinterpret_cast<uint4*>(smem + i) = make_uint4(~0u, ~0u, ~0u, ~0u);
+  __syncthreads();
+}
+
+// Warps 0-3 (one TMEM lane quarter each) fill `cols` columns from `tmem`.
+__device__ __forceinline__ void debug_poison_tmem(uint32_t tmem, uint32_t cols, int warp) {
+  if (warp < 4) {
+    uint32_t v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = ~0u;
+    const uint32_t t = tmem + ((uint32_t)(warp * 32) << 16);
+    for (uint32_t c = 0; c < cols; c += 16) tmem_st16(t + c, v);
+    tmem_wait_st();
+  }
+}
+
+#define PA_DEBUG_PROLOGUE(smem, bytes, p, begin, end)   \
+  do {                                                   \
+    if (!pa::debug_items_ok((p), (begin), (end))) return; \
+    pa::debug_poison_smem((smem), (bytes));              \
+  } while (0)
+#define PA_DEBUG_POISON_TMEM(tmem, cols, warp)          \
+  do {                                                   \
+    pa::debug_poison_tmem((tmem), (cols), (warp));       \
+    pa::tc_fence_before();                               \
+    __syncthreads();                                     \
+    pa::tc_fence_after();                                \
+  } while (0)
+#else
+#define PA_DEBUG_PROLOGUE(smem, bytes, p, begin, end) ((void)0)
+#define PA_DEBUG_POISON_TMEM(tmem, cols, warp) ((void)0)
+#endif
+
 // Scale value `idx` (kv head or kv_head * D + channel) of a bf16 scale array,
 // or the single fp32 global scale.
 __device__ __forceinline__ float load_scale(const void* s, int kind, int idx) {
@@ -68,6 +121,29 @@ __device__ __forceinline__ Item load_item(const int32_t* items, int it) {
   const int4* r = reinterpret_cast<const int4*>(items + (int64_t)it * kItemWords);
   return item_from<TILE>(r[0], r[1]);
 }
+
+#ifdef PA_DEBUG
+// The CTA's items [begin, end) against the problem (all threads call it; the
+// result is the same in every thread, and in both CTAs of an MLA pair).
+static __device__ __noinline__ bool debug_items_ok(const AttnParams& p, int begin, int end) {
+  bool bad = begin < 0 || end < begin || end > p.num_items;
+  for (int it = begin + (int)threadIdx.x; !bad && it < end; it += (int)blockDim.x) {
+    const Item m = load_item<1>(p.items, it);
+    const bool ok = m.b >= 0 && m.b < p.bsz && m.kvh >= 0 && m.kvh < p.kv_heads && m.tok0 >= 0 &&
+                    m.ntok >= 1 && m.tok0 + m.ntok <= p.total_q && m.cbase >= 0 && m.kv0 >= 0 &&
+                    m.kv0 <= m.kv1 && (int64_t)m.kv1 <= (int64_t)p.max_blocks * kDebugPage &&
+                    m.nch >= 1 && m.chunk >= 0 && m.chunk < m.nch &&
+                    (m.nch == 1 || m.nch <= p.max_chunks);
+    if (!ok) {
+      record_status(p.status, PA_ERR_BAD_ITEM, it);
+      bad = true;
+    }
+  }
+  if (bad && threadIdx.x == 0 && (begin < 0 || end < begin || end > p.num_items))
+    record_status(p.status, PA_ERR_BAD_ITEM, -1);
+  return __syncthreads_or(bad) == 0;
+}
+#endif
 
 // Output epilogue of one element (index = q_head * Dv + dim into shift / smooth).
 __device__ __forceinline__ float ep_value(const OutEpilogue& e, float v, int idx) {

@@ -269,6 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int item_end = p.work_indptr[blockIdx.x + 1];
   const uint64_t limit = (uint64_t)p.wait_limit_ns;
   const int G = p.group;
+  PA_DEBUG_PROLOGUE(smem, SM::kTotal - 1024, p, item_begin, item_end);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -311,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  PA_DEBUG_POISON_TMEM(tmem, kTmemCols, warp);
   // this warp's TMEM lane quarter (a warp may only touch lanes 32*(warp%4) ..)
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 

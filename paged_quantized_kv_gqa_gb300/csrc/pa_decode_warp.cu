@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(WCfg<NB>::kWarps * 32, 1)
   const int sc_n = p.scale_kind == PA_SCALE_PER_CHANNEL ? kvh_count * kWDim
                    : p.scale_kind == PA_SCALE_PER_KV_HEAD ? kvh_count : 0;
   const bool sc_smem = sc_n > 0 && sc_n * 2 <= kWScaleBytes / 2;
+  PA_DEBUG_PROLOGUE(smem, C::kTotal - 1024, p, item_begin, item_end);
   if (threadIdx.x == 0) {
     for (int w = 0; w < C::kWarps; ++w)
       for (int s = 0; s < C::kStages; ++s)

@@ -124,6 +124,9 @@ struct AttnParams {
   uint64_t* trace;       // [trace_ctas][trace_tiles][16] %globaltimer stamps, or null
   int32_t trace_ctas;
   int32_t trace_tiles;
+  int32_t bsz;           // bounds of the work items (checked by the debug build)
+  int32_t total_q;
+  int32_t num_items;
 };
 
 void set_error(const std::string& msg);

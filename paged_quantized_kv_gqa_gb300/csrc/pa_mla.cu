@@ -159,6 +159,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const float gscale = load_scale(p.k_scale, PA_SCALE_GLOBAL, 0);
   const int stages = rank == 0 ? kStages0 : kStages1;
 
+  PA_DEBUG_PROLOGUE(smem, SM::kTotal - 1024, p, item_begin, item_end);
   if (tid == 0) {
     for (int s = 0; s < 3; ++s) {
       mbar_init(&full[s], 1);
@@ -193,6 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   cluster_sync();   // both CTAs' barriers are initialised before any remote access
   const uint32_t tmem = *tmem_slot;
+  PA_DEBUG_POISON_TMEM(tmem, kTmemCols, warp);
   const uint32_t t_lane = tmem + ((uint32_t)((warp & 3) * 32) << 16);
   const uint32_t peer_abort = mapa_shared(smem_u32((const void*)abort_any), peer);
   auto raise_abort = [&](int code, int it) {

@@ -75,6 +75,8 @@ def compare(case, out, lse, units=None, label="", ref=None):
     assert rows.any(), "nothing compared"
     o = out[rows]
     r = ref_o[rows]
+    # a NaN would compare false against the tolerance below
+    assert np.isfinite(o).all(), f"{label}: {int((~np.isfinite(o)).sum())} non-finite output elements"
     err = np.abs(o - r)
     tol = OUT_ATOL + OUT_RTOL * np.abs(r)
     bad = err > tol
