@@ -117,7 +117,7 @@ NCU_TRAFFIC = {
     # states written both grow per sequence
     "spec-verify-4": (("pa_decode.cu", "pa_index.cuh", "pa_merge.cuh"), "3545fe789aae18a8",
                       (729.481728e6 + 31.898112e6) * 7.492152264116904),
-    "append-3": (("pa_append.cu",), "1d5e961f8bec2af9", 72.213760e6 + 1.729536e6),
+    "append-3": (("pa_append.cu",), "a9cbfbb7a3133fa5", 72.280576e6 + 2.418432e6),
     "mla-5": (("pa_mla.cu",), "bdf0753cd25ebc74", 224.310784e6 + 6.930432e6),
 }
 

@@ -28,7 +28,7 @@
 //                   the B operand of S (rows = positions), V^T as the B operand
 //                   of PV (rows = head dims, which is the cache's own V layout);
 //       IO          one TMA warp (the item's Q rows as a 3-D box, K and V page
-//                   slabs into a 4-stage ring) and two MMA-issue warps: one
+//                   slabs into a 6-stage ring) and two MMA-issue warps: one
 //                   issues S of both query tiles (up to two pages ahead), the
 //                   other PV, so neither waits behind the other's MMAs.
 //   * Ordering rules: S_X into buffer b waits for the PV_X that read P_X from b;
@@ -50,7 +50,9 @@ constexpr int kPage = 64;
 constexpr int kRows = 256;                       // packed query rows per item
 constexpr int kSlab = kPage * kHeadDim;          // bytes of one (page, head) K or V slab
 constexpr int kStageBytes = 2 * kSlab;           // K slab + V slab
-constexpr int kStages = 4;
+// Page-slab ring depth: six stages measured 1-1.5 % faster than four or five
+// on append-3 (0.1393 -> 0.1372-0.1382 ms); they fill shared memory to 225 KB.
+constexpr int kStages = 6;
 constexpr int kK16Bytes = kTile * 256;           // [2 dim halves][64 positions][128 B]
 constexpr int kV16Bytes = kHeadDim * 128;        // [128 dims][64 positions x 2 B]
 constexpr float kTau = 8.0f;                     // lazy-rescale threshold (log2 units)
