@@ -63,6 +63,41 @@ def test_planner_matches_oracle(pa, kw, sms):
         assert np.array_equal(got[key], want[key]), key
 
 
+def _random_problem(r):
+    """A seeded random problem of one of the three families: lengths with
+    zeros, ragged query counts, every chunk rule, causal or not."""
+    fam = r.choice(["decode", "append", "mla"])
+    bsz = int(r.integers(1, 9))
+    if fam == "mla":
+        kw = dict(q_heads=128, kv_heads=1, head_dim_qk=576, head_dim_v=512, kv_dtype="fp8_e4m3",
+                  scale_kind="global", layout="mla")
+        q = r.integers(1, 3, bsz)
+    else:
+        kvh = int(r.choice([1, 2, 4, 8]))
+        kw = dict(q_heads=kvh * int(r.choice([1, 2, 4, 8])), kv_heads=kvh)
+        q = r.integers(0, 5, bsz) if fam == "decode" else r.integers(0, 200, bsz)
+    q[int(r.integers(0, bsz))] = max(1, int(q.max()))    # at least one query token
+    kv = r.integers(0, 6000, bsz)
+    kv[r.random(bsz) < 0.2] = 0
+    kw.update(seq_lens=q.tolist(), seq_lens_kv=kv.tolist(), causal=bool(r.random() < 0.8),
+              chunk_size=int(r.choice([0, 64, 128, 512, 1024, -1])))
+    return kw
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_planner_matches_oracle_random(pa, seed):
+    r = np.random.default_rng(1000 + seed)
+    kw = _random_problem(r)
+    sms = int(r.choice([1, 3, 8, 152]))
+    case = synth.make_case(name="p", seed=seed, **kw)
+    got = _plan(pa, case, sms).describe()
+    want = op.plan(case, sms)
+    for key in ("family", "chunk", "tokens_per_tile", "num_ctas", "max_chunks"):
+        assert got[key] == want[key], (key, kw, sms)
+    for key in ("items", "work_indptr", "nch_token", "merge_tokens"):
+        assert np.array_equal(got[key], want[key]), (key, kw, sms)
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_planner_matches_oracle_on_workloads(pa, n):
     case = synth.config(n) if n != 3 and n != 5 else _light(n)
