@@ -98,6 +98,31 @@ def test_planner_matches_oracle_random(pa, seed):
         assert np.array_equal(got[key], want[key]), (key, kw, sms)
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_plan_work_counts_match_the_oracle_mask(pa, seed):
+    """The plan's flops (the numerator of the append / MLA TFLOP/s figures) are
+    2 (Dqk + Dv) per visible (query head, position) pair: counted here from
+    the oracle's own visibility mask; kv_bytes are the whole pages the
+    sequences occupy."""
+    from oracle.attention import _visible
+    r = np.random.default_rng(2000 + seed)
+    kw = _random_problem(r)
+    case = synth.make_case(name="w", seed=seed, **kw)
+    d = _plan(pa, case, 152).describe()
+    pairs = 0
+    pages = 0
+    for b in range(len(case.seq_lens)):
+        q, kvtot = int(case.seq_lens[b]), int(case.seq_lens_kv[b]) + int(case.seq_lens[b])
+        if q == 0:
+            continue
+        pairs += int(_visible(case, b, q, kvtot, 0, kvtot).sum())
+        pages += -(-kvtot // 64)
+    per_pair = case.q_heads * 2 * (case.head_dim_qk + case.head_dim_v)
+    assert d["flops"] == pairs * per_pair, kw
+    row = case.head_dim_qk if case.layout == "mla" else (case.head_dim_qk + case.head_dim_v) * case.kv_heads
+    assert d["kv_bytes"] == pages * 64 * row, kw
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_planner_matches_oracle_on_workloads(pa, n):
     case = synth.config(n) if n != 3 and n != 5 else _light(n)
