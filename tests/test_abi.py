@@ -123,6 +123,25 @@ def test_plan_work_counts_match_the_oracle_mask(pa, seed):
     assert d["kv_bytes"] == pages * 64 * row, kw
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_bench_kv_bytes_are_the_visible_rows_read_once(seed):
+    """bench.py's GB/s numerator: every (sequence, kv head) reads the K and V
+    rows of the positions any of its query tokens sees, once (MLA: the
+    576-byte latent row, V being its prefix), counted from the oracle mask."""
+    import bench
+    from oracle.attention import _visible
+    r = np.random.default_rng(3000 + seed)
+    case = synth.make_case(name="w", seed=seed, **_random_problem(r))
+    rows = 0
+    for b in range(len(case.seq_lens)):
+        q, kvtot = int(case.seq_lens[b]), int(case.seq_lens_kv[b]) + int(case.seq_lens[b])
+        if q == 0:
+            continue
+        rows += int(_visible(case, b, q, kvtot, 0, kvtot).any(axis=0).sum())
+    per_row = case.head_dim_qk if case.layout == "mla" else (case.head_dim_qk + case.head_dim_v) * case.kv_heads
+    assert bench.algorithmic_bytes(case) == rows * per_row
+
+
 @pytest.mark.parametrize("n", [1, 2, 3, 4, 5])
 def test_planner_matches_oracle_on_workloads(pa, n):
     case = synth.config(n) if n != 3 and n != 5 else _light(n)
